@@ -1,0 +1,407 @@
+// extern "C" entry points of libmxfp4 (declared in include/mxfp4.h): argument
+// validation, per-device facts, the TMA descriptor cache, workspace layout and
+// path selection. Nothing here allocates device memory or synchronizes.
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include "internal.h"
+#include "mxfp4.h"
+
+using namespace mxfp4;
+
+namespace {
+
+// Split-K and path plans assume this many SMs so that the workspace size is a
+// function of the shape alone (GB300 has 152; fewer SMs only change occupancy).
+constexpr int kPlanSms = 152;
+constexpr int kMaxSplitK = 16;
+
+// --------------------------------------------------------------- device info
+struct DevInfo {
+    bool probed = false;
+    bool supported = false;
+    int sms = 0;
+};
+std::mutex g_dev_mu;
+DevInfo g_dev[64];
+
+mxfp4_status_t current_device(int *sms)
+{
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess) return MXFP4_ERR_NO_DEVICE;
+    if (d < 0 || d >= 64) return MXFP4_ERR_NO_DEVICE;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DevInfo &di = g_dev[d];
+    if (!di.probed) {
+        int major = 0, minor = 0, n = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, d) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, d) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess)
+            return MXFP4_ERR_NO_DEVICE;
+        di.supported = (major == 10 && minor == 3);
+        di.sms = n;
+        di.probed = true;
+    }
+    if (!di.supported) return MXFP4_ERR_NO_DEVICE;
+    *sms = di.sms;
+    return MXFP4_OK;
+}
+
+// ------------------------------------------------------- TMA descriptor cache
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool encoder()
+{
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+struct MapKey {
+    uintptr_t ptr;
+    int64_t inner, rows, stride;
+    int box_rows, dev;
+    bool operator==(const MapKey &o) const
+    {
+        return ptr == o.ptr && inner == o.inner && rows == o.rows && stride == o.stride &&
+               box_rows == o.box_rows && dev == o.dev;
+    }
+};
+struct MapKeyHash {
+    size_t operator()(const MapKey &k) const
+    {
+        uint64_t h = 1469598103934665603ull;
+        auto mix = [&](uint64_t v) { h = (h ^ v) * 1099511628211ull; };
+        mix(k.ptr);
+        mix(static_cast<uint64_t>(k.inner));
+        mix(static_cast<uint64_t>(k.rows));
+        mix(static_cast<uint64_t>(k.stride));
+        mix(static_cast<uint64_t>(k.box_rows));
+        mix(static_cast<uint64_t>(k.dev));
+        return static_cast<size_t>(h);
+    }
+};
+std::mutex g_map_mu;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+
+// Tensor map of a packed FP4 matrix [rows, inner bytes] (row stride `stride`
+// bytes), box {128 bytes, box_rows}, 128-byte swizzle, zero fill out of bounds.
+mxfp4_status_t fp4_map(const void *base, int64_t inner, int64_t rows, int64_t stride, int box_rows,
+                       CUtensorMap *out)
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    MapKey key{reinterpret_cast<uintptr_t>(base), inner, rows, stride, box_rows, dev};
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        auto it = g_maps.find(key);
+        if (it != g_maps.end()) {
+            *out = it->second;
+            return MXFP4_OK;
+        }
+    }
+    if (!encoder()) return MXFP4_ERR_CUDA;
+    CUtensorMap tm;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(stride)};
+    cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = g_encode(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return MXFP4_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    if (g_maps.size() > 4096) g_maps.clear();
+    g_maps.emplace(key, tm);
+    *out = tm;
+    return MXFP4_OK;
+}
+
+// ------------------------------------------------------------- validation
+inline bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+mxfp4_status_t check_quant(const void *A, int64_t M, int64_t K, int64_t lda, const void *Aq, int64_t ldq,
+                           const void *sf, int vec)
+{
+    if (!A || !Aq || !sf) return MXFP4_ERR_INVALID_ARG;
+    if (M < 1 || K < 1 || M > kMaxDim || K > kMaxDim) return MXFP4_ERR_INVALID_ARG;
+    if (K % vec != 0) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+    if (lda < K || ldq < K / 2) return MXFP4_ERR_INVALID_ARG;
+    if ((lda * 2) % 16 != 0 || ldq % 16 != 0) return MXFP4_ERR_MISALIGNED;
+    if (!al16(A) || !al16(Aq) || !al16(sf)) return MXFP4_ERR_MISALIGNED;
+    return MXFP4_OK;
+}
+
+mxfp4_status_t check_gemm_common(const void *Bq, int64_t ldbq, const void *B_sf, const void *C, int64_t ldc,
+                                 int64_t M, int64_t N, int64_t K)
+{
+    if (!Bq || !B_sf || !C) return MXFP4_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return MXFP4_ERR_INVALID_ARG;
+    if (K % 32 != 0) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+    if (ldbq < K / 2 || ldc < N) return MXFP4_ERR_INVALID_ARG;
+    if (ldbq % 16 != 0 || (ldc * 2) % 16 != 0) return MXFP4_ERR_MISALIGNED;
+    if (!al16(Bq) || !al16(B_sf) || !al16(C)) return MXFP4_ERR_MISALIGNED;
+    return MXFP4_OK;
+}
+
+inline mxfp4_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA; }
+
+// --------------------------------------------------------- workspace layout
+inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t sf_bytes(int64_t rows, int64_t k, int vec)
+{
+    return static_cast<size_t>((rows + 127) / 128) * static_cast<size_t>((k / vec + 3) / 4) * 512;
+}
+
+struct GemmPlan {
+    int splits;
+    int tiles;
+    int n_tiles;
+};
+
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K)
+{
+    const int bn = gemm_block_n(false);
+    GemmPlan p;
+    const int64_t m_tiles = (M + 127) / 128;
+    p.n_tiles = static_cast<int>((N + bn - 1) / bn);
+    p.tiles = static_cast<int>(m_tiles * p.n_tiles);
+    const int64_t k_stages = (K + 255) / 256;
+    int64_t s = 1;
+    if (2 * p.tiles <= kPlanSms && k_stages >= 4) {
+        s = kPlanSms / p.tiles;
+        if (s > k_stages / 2) s = k_stages / 2;
+        if (s > kMaxSplitK) s = kMaxSplitK;
+        // keep the fp32 partial traffic well below the weight bytes
+        while (s > 1 && s * M * N * 4 > N * (K / 2) / 2) --s;
+        if (s < 1) s = 1;
+    }
+    p.splits = static_cast<int>(s);
+    return p;
+}
+
+struct WsLayout {
+    size_t aq_off, sf_off, part_off, ticket_off, total;
+    int64_t ldq;
+};
+
+WsLayout ws_layout(int64_t M, int64_t N, int64_t K)
+{
+    WsLayout w;
+    w.ldq = ((K / 2) + 15) / 16 * 16;
+    const GemmPlan gp = plan_gemm(M, N, K);
+    const int bn = gemm_block_n(false);
+    w.aq_off = 0;
+    w.sf_off = up256(static_cast<size_t>(M) * w.ldq);
+    w.part_off = w.sf_off + up256(sf_bytes(M, K, 32));
+    size_t part = 0;
+    if (gp.splits > 1) part = static_cast<size_t>(gp.splits) * gp.n_tiles * bn * static_cast<size_t>(M) * 4;
+    w.ticket_off = w.part_off + up256(part);
+    w.total = w.ticket_off + up256(static_cast<size_t>(gp.tiles) * 4);
+    return w;
+}
+
+mxfp4_status_t run_gemm(const void *Aq, int64_t ldaq, const void *A_sf, const void *Bq, int64_t ldbq,
+                        const void *B_sf, void *C, int64_t ldc, int64_t M, int64_t N, int64_t K, void *ws,
+                        const WsLayout &wl, cudaStream_t stream)
+{
+    GemmProblemHost h;
+    memset(&h, 0, sizeof(h));
+    mxfp4_status_t st = fp4_map(Aq, K / 2, M, ldaq, 128, &h.tma);
+    if (st != MXFP4_OK) return st;
+    st = fp4_map(Bq, K / 2, N, ldbq, gemm_block_n(false), &h.tmb);
+    if (st != MXFP4_OK) return st;
+    h.sfa = static_cast<const uint8_t *>(A_sf);
+    h.sfb = static_cast<const uint8_t *>(B_sf);
+    h.c = C;
+    h.ldc = ldc;
+    h.m = static_cast<int>(M);
+    h.n = static_cast<int>(N);
+    h.k = static_cast<int>(K);
+    const GemmPlan gp = plan_gemm(M, N, K);
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    float *part = gp.splits > 1 ? reinterpret_cast<float *>(w + wl.part_off) : nullptr;
+    int *tickets = reinterpret_cast<int *>(w + wl.ticket_off);
+    return cuda_status(launch_gemm_mx(h, gp.splits, part, tickets, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *mxfp4_status_string(mxfp4_status_t s)
+{
+    switch (s) {
+    case MXFP4_OK: return "MXFP4_OK";
+    case MXFP4_ERR_INVALID_ARG: return "MXFP4_ERR_INVALID_ARG";
+    case MXFP4_ERR_UNSUPPORTED_SHAPE: return "MXFP4_ERR_UNSUPPORTED_SHAPE";
+    case MXFP4_ERR_MISALIGNED: return "MXFP4_ERR_MISALIGNED";
+    case MXFP4_ERR_WORKSPACE_TOO_SMALL: return "MXFP4_ERR_WORKSPACE_TOO_SMALL";
+    case MXFP4_ERR_CUDA: return "MXFP4_ERR_CUDA";
+    case MXFP4_ERR_DEVICE_TIMEOUT: return "MXFP4_ERR_DEVICE_TIMEOUT";
+    case MXFP4_ERR_NO_DEVICE: return "MXFP4_ERR_NO_DEVICE";
+    }
+    return "MXFP4_UNKNOWN_STATUS";
+}
+
+int mxfp4_abi_version(void) { return 1; }
+
+size_t mxfp4_sf_bytes(int64_t rows, int64_t k, int vec)
+{
+    if ((vec != 16 && vec != 32) || rows < 1 || k < 1 || k % vec != 0) return 0;
+    return sf_bytes(rows, k, vec);
+}
+
+size_t mxfp4_workspace_bytes(int64_t M, int64_t N, int64_t K)
+{
+    if (M < 1 || N < 1 || K < 1 || K % 32 != 0) return 0;
+    return ws_layout(M, N, K).total;
+}
+
+size_t nvfp4_group_workspace_bytes(int num_groups)
+{
+    (void)num_groups;
+    return 0;
+}
+
+mxfp4_status_t mxfp4_quantize(const void *A, int64_t M, int64_t K, int64_t lda, void *Aq, int64_t ldq,
+                              void *A_sf, void *stream)
+{
+    mxfp4_status_t st = check_quant(A, M, K, lda, Aq, ldq, A_sf, 32);
+    if (st != MXFP4_OK) return st;
+    int sms = 0;
+    st = current_device(&sms);
+    if (st != MXFP4_OK) return st;
+    return cuda_status(launch_quant_mx(A, M, K, lda, Aq, ldq, A_sf, sms, static_cast<cudaStream_t>(stream)));
+}
+
+mxfp4_status_t nvfp4_quantize(const void *A, int64_t M, int64_t K, int64_t lda, void *Aq, int64_t ldq,
+                              void *A_sf, void *stream)
+{
+    mxfp4_status_t st = check_quant(A, M, K, lda, Aq, ldq, A_sf, 16);
+    if (st != MXFP4_OK) return st;
+    int sms = 0;
+    st = current_device(&sms);
+    if (st != MXFP4_OK) return st;
+    return cuda_status(launch_quant_nv(A, M, K, lda, Aq, ldq, A_sf, sms, static_cast<cudaStream_t>(stream)));
+}
+
+mxfp4_status_t mxfp4_gemm_a4w4(const void *Aq, int64_t ldaq, const void *A_sf, const void *Bq, int64_t ldbq,
+                               const void *B_sf, void *C, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                               void *workspace, size_t ws_bytes, void *stream)
+{
+    mxfp4_status_t st = check_gemm_common(Bq, ldbq, B_sf, C, ldc, M, N, K);
+    if (st != MXFP4_OK) return st;
+    if (!Aq || !A_sf || !workspace) return MXFP4_ERR_INVALID_ARG;
+    if (ldaq < K / 2) return MXFP4_ERR_INVALID_ARG;
+    if (ldaq % 16 != 0 || !al16(Aq) || !al16(A_sf) || !al16(workspace)) return MXFP4_ERR_MISALIGNED;
+    const WsLayout wl = ws_layout(M, N, K);
+    if (ws_bytes < wl.total) return MXFP4_ERR_WORKSPACE_TOO_SMALL;
+    int sms = 0;
+    st = current_device(&sms);
+    if (st != MXFP4_OK) return st;
+    return run_gemm(Aq, ldaq, A_sf, Bq, ldbq, B_sf, C, ldc, M, N, K, workspace, wl,
+                    static_cast<cudaStream_t>(stream));
+}
+
+mxfp4_status_t mxfp4_quant_gemm_fused(const void *A, int64_t lda, const void *Bq, int64_t ldbq, const void *B_sf,
+                                      void *C, int64_t ldc, int64_t M, int64_t N, int64_t K, void *workspace,
+                                      size_t ws_bytes, void *stream)
+{
+    mxfp4_status_t st = check_gemm_common(Bq, ldbq, B_sf, C, ldc, M, N, K);
+    if (st != MXFP4_OK) return st;
+    if (!A || !workspace) return MXFP4_ERR_INVALID_ARG;
+    if (lda < K) return MXFP4_ERR_INVALID_ARG;
+    if ((lda * 2) % 16 != 0 || !al16(A) || !al16(workspace)) return MXFP4_ERR_MISALIGNED;
+    const WsLayout wl = ws_layout(M, N, K);
+    if (ws_bytes < wl.total) return MXFP4_ERR_WORKSPACE_TOO_SMALL;
+    int sms = 0;
+    st = current_device(&sms);
+    if (st != MXFP4_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    FusedPlan fp;
+    if (plan_fused(M, N, K, sms, &fp)) {
+        CUtensorMap tmw;
+        st = fp4_map(Bq, K / 2, N, ldbq, 128, &tmw);
+        if (st != MXFP4_OK) return st;
+        return cuda_status(launch_fused_mx(tmw, A, lda, static_cast<const uint8_t *>(B_sf), C, ldc,
+                                           static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), fp, s));
+    }
+    // two-kernel path: quantize A into the workspace, then the GEMM
+    uint8_t *w = static_cast<uint8_t *>(workspace);
+    void *aq = w + wl.aq_off;
+    void *asf = w + wl.sf_off;
+    st = cuda_status(launch_quant_mx(A, M, K, lda, aq, wl.ldq, asf, sms, s));
+    if (st != MXFP4_OK) return st;
+    return run_gemm(aq, wl.ldq, asf, Bq, ldbq, B_sf, C, ldc, M, N, K, workspace, wl, s);
+}
+
+mxfp4_status_t nvfp4_group_gemm(const nvfp4_problem_t *problems, int num_groups, void *workspace, size_t ws_bytes,
+                                void *stream)
+{
+    (void)workspace;
+    (void)ws_bytes;
+    if (!problems || num_groups < 1) return MXFP4_ERR_INVALID_ARG;
+    if (num_groups > NVFP4_MAX_GROUPS) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+    GemmProblemHost hp[kMaxGroups];
+    memset(hp, 0, sizeof(hp));
+    int64_t total_tiles = 0;
+    const int bn = gemm_block_n(true);
+    for (int g = 0; g < num_groups; ++g) {
+        const nvfp4_problem_t &p = problems[g];
+        if (!p.a || !p.sfa || !p.b || !p.sfb || !p.c) return MXFP4_ERR_INVALID_ARG;
+        if (p.m < 1 || p.n < 1 || p.k < 1 || p.m > kMaxDim || p.n > kMaxDim || p.k > kMaxDim)
+            return MXFP4_ERR_INVALID_ARG;
+        if (p.k % 16 != 0) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+        if (p.lda < p.k / 2 || p.ldb < p.k / 2 || p.ldc < p.n) return MXFP4_ERR_INVALID_ARG;
+        if (p.lda % 16 != 0 || p.ldb % 16 != 0 || (p.ldc * 2) % 16 != 0) return MXFP4_ERR_MISALIGNED;
+        if (!al16(p.a) || !al16(p.sfa) || !al16(p.b) || !al16(p.sfb) || !al16(p.c)) return MXFP4_ERR_MISALIGNED;
+        total_tiles += ((p.m + 127) / 128) * ((p.n + bn - 1) / bn);
+    }
+    if (total_tiles > kMaxDim) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+    int sms = 0;
+    mxfp4_status_t st = current_device(&sms);
+    if (st != MXFP4_OK) return st;
+    for (int g = 0; g < num_groups; ++g) {
+        const nvfp4_problem_t &p = problems[g];
+        st = fp4_map(p.a, p.k / 2, p.m, p.lda, 128, &hp[g].tma);
+        if (st != MXFP4_OK) return st;
+        st = fp4_map(p.b, p.k / 2, p.n, p.ldb, bn, &hp[g].tmb);
+        if (st != MXFP4_OK) return st;
+        hp[g].sfa = static_cast<const uint8_t *>(p.sfa);
+        hp[g].sfb = static_cast<const uint8_t *>(p.sfb);
+        hp[g].c = p.c;
+        hp[g].ldc = p.ldc;
+        hp[g].m = static_cast<int>(p.m);
+        hp[g].n = static_cast<int>(p.n);
+        hp[g].k = static_cast<int>(p.k);
+    }
+    return cuda_status(launch_gemm_nv_grouped(hp, num_groups, static_cast<cudaStream_t>(stream)));
+}
+
+mxfp4_status_t mxfp4_get_device_error(int *code)
+{
+    if (!code) return MXFP4_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return MXFP4_ERR_CUDA;
+    const int g = read_and_clear_gemm_error();
+    const int f = read_and_clear_fused_error();
+    if (g < 0 || f < 0) return MXFP4_ERR_CUDA;
+    *code = g != 0 ? g : (f != 0 ? 16 + f : 0);
+    return MXFP4_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,56 @@
+// Host-side interface between the C-ABI layer (api.cu) and the kernel
+// translation units. Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mxfp4 {
+
+constexpr int kMaxGroups = 16;
+
+// ---------------------------------------------------------------- quant.cu
+cudaError_t launch_quant_mx(const void *A, int64_t M, int64_t K, int64_t lda, void *Aq,
+                            int64_t ldq, void *sf, int num_sms, cudaStream_t stream);
+cudaError_t launch_quant_nv(const void *A, int64_t M, int64_t K, int64_t lda, void *Aq,
+                            int64_t ldq, void *sf, int num_sms, cudaStream_t stream);
+
+// ----------------------------------------------------------------- gemm.cu
+// One GEMM problem as the tile scheduler sees it.
+struct GemmProblemHost {
+    CUtensorMap tma;          // packed A [m, k/2] u8, box {128 B, 128 rows}, 128B swizzle
+    CUtensorMap tmb;          // packed B [n, k/2] u8, box {128 B, bn rows}, 128B swizzle
+    const uint8_t *sfa;       // blocked scales of A
+    const uint8_t *sfb;       // blocked scales of B
+    void *c;                  // bf16 (MXFP4) or fp16 (NVFP4) [m, n]
+    int64_t ldc;              // elements
+    int m, n, k;
+};
+
+// Tile width along N used by the MXFP4 / NVFP4 GEMM kernels (box rows of tmb).
+int gemm_block_n(bool nvfp4);
+
+// MXFP4 (kind::mxf4, bf16 C). splits > 1 needs `partials` (splits*tiles*bn*128
+// floats) and zeroed `tickets` (tiles ints).
+cudaError_t launch_gemm_mx(const GemmProblemHost &prob, int splits, float *partials,
+                           int *tickets, cudaStream_t stream);
+// Grouped NVFP4 (kind::mxf4nvf4, fp16 C), one launch over all groups.
+cudaError_t launch_gemm_nv_grouped(const GemmProblemHost *probs, int num_groups,
+                                   cudaStream_t stream);
+int read_and_clear_gemm_error();
+
+// ---------------------------------------------------------------- fused.cu
+struct FusedPlan {
+    int mma_n;       // activation rows padded to the MMA N
+    int splits;      // K splits = cluster size
+    int n_tiles;     // ceil(N / 128)
+};
+// Whether the fused small-M kernel can run (M, K) and with which plan.
+bool plan_fused(int64_t M, int64_t N, int64_t K, int num_sms, FusedPlan *plan);
+cudaError_t launch_fused_mx(const CUtensorMap &tmb, const void *A, int64_t lda,
+                            const uint8_t *sfb, void *C, int64_t ldc, int M, int N, int K,
+                            const FusedPlan &plan, cudaStream_t stream);
+int read_and_clear_fused_error();
+
+}  // namespace mxfp4

@@ -1,0 +1,216 @@
+"""Python binding of libmxfp4 (the C ABI in include/mxfp4.h).
+
+Argument marshalling only: every function passes device pointers, sizes and the
+current CUDA stream to the library entry point of the same name and raises
+``Mxfp4Error`` on a non-OK status. All arithmetic runs in the library's CUDA
+kernels; there is no fallback. If the library has not been built, importing
+this module raises immediately.
+"""
+import ctypes
+import os
+import re
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libmxfp4.so")
+HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "mxfp4.h")
+
+_i64 = ctypes.c_int64
+_p = ctypes.c_void_p
+_sz = ctypes.c_size_t
+_st = ctypes.c_int
+
+STATUS = {
+    0: "MXFP4_OK", 1: "MXFP4_ERR_INVALID_ARG", 2: "MXFP4_ERR_UNSUPPORTED_SHAPE",
+    3: "MXFP4_ERR_MISALIGNED", 4: "MXFP4_ERR_WORKSPACE_TOO_SMALL", 5: "MXFP4_ERR_CUDA",
+    6: "MXFP4_ERR_DEVICE_TIMEOUT", 7: "MXFP4_ERR_NO_DEVICE",
+}
+NVFP4_MAX_GROUPS = 16
+
+
+class Mxfp4Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+class NvProblem(ctypes.Structure):
+    """nvfp4_problem_t."""
+    _fields_ = [("m", _i64), ("n", _i64), ("k", _i64),
+                ("a", _p), ("sfa", _p), ("b", _p), ("sfb", _p), ("c", _p),
+                ("lda", _i64), ("ldb", _i64), ("ldc", _i64)]
+
+
+def _load(path: str = LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(
+            f"libmxfp4.so is not built ({path} missing); run __graft_entry__.build() "
+            "or python block_scaled_fp4_mxfp4_gb300/build.py")
+    L = ctypes.CDLL(path)
+    L.mxfp4_status_string.restype = ctypes.c_char_p
+    L.mxfp4_status_string.argtypes = [_st]
+    L.mxfp4_abi_version.restype = ctypes.c_int
+    L.mxfp4_abi_version.argtypes = []
+    L.mxfp4_sf_bytes.restype = _sz
+    L.mxfp4_sf_bytes.argtypes = [_i64, _i64, ctypes.c_int]
+    L.mxfp4_workspace_bytes.restype = _sz
+    L.mxfp4_workspace_bytes.argtypes = [_i64, _i64, _i64]
+    L.nvfp4_group_workspace_bytes.restype = _sz
+    L.nvfp4_group_workspace_bytes.argtypes = [ctypes.c_int]
+    for name in ("mxfp4_quantize", "nvfp4_quantize"):
+        f = getattr(L, name)
+        f.restype = _st
+        f.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p, _p]
+    L.mxfp4_gemm_a4w4.restype = _st
+    L.mxfp4_gemm_a4w4.argtypes = [_p, _i64, _p, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p, _sz, _p]
+    L.mxfp4_quant_gemm_fused.restype = _st
+    L.mxfp4_quant_gemm_fused.argtypes = [_p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p, _sz, _p]
+    L.nvfp4_group_gemm.restype = _st
+    L.nvfp4_group_gemm.argtypes = [ctypes.POINTER(NvProblem), ctypes.c_int, _p, _sz, _p]
+    L.mxfp4_get_device_error.restype = _st
+    L.mxfp4_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    return L
+
+
+_lib = _load()
+
+
+def lib() -> ctypes.CDLL:
+    return _lib
+
+
+def declared_symbols(header: str = HEADER_PATH):
+    """Names of the entry points include/mxfp4.h declares."""
+    with open(header) as f:
+        text = f.read()
+    return re.findall(r"MXFP4_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise Mxfp4Error(status, where)
+
+
+def _stream_ptr(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, ndim=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+    if t.dim() == 2 and t.stride(1) != 1:
+        raise ValueError(f"{name} must be row-major with unit inner stride")
+    return t
+
+
+# ---------------------------------------------------------------- sizes --
+
+def sf_bytes(rows: int, k: int, vec: int) -> int:
+    return int(_lib.mxfp4_sf_bytes(rows, k, vec))
+
+
+def workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(_lib.mxfp4_workspace_bytes(M, N, K))
+
+
+def new_workspace(M: int, N: int, K: int, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace for (M, N, K) (the library keeps it zeroed)."""
+    return torch.zeros(max(1, workspace_bytes(M, N, K)), dtype=torch.uint8, device=device)
+
+
+# --------------------------------------------------------- quantization --
+
+def _quant(fn, vec, A, Aq, A_sf, stream, where):
+    _dev(A, "A", torch.bfloat16, 2)
+    M, K = A.shape
+    if Aq is None:
+        Aq = torch.empty((M, K // 2), dtype=torch.uint8, device=A.device)
+    if A_sf is None:
+        A_sf = torch.empty(max(1, sf_bytes(M, K, vec)), dtype=torch.uint8, device=A.device)
+    _dev(Aq, "Aq", torch.uint8, 2)
+    _dev(A_sf, "A_sf", torch.uint8)
+    _check(fn(A.data_ptr(), M, K, A.stride(0), Aq.data_ptr(), Aq.stride(0), A_sf.data_ptr(),
+              _stream_ptr(stream)), where)
+    return Aq, A_sf
+
+
+def mxfp4_quantize(A, Aq=None, A_sf=None, stream=None):
+    """bf16 A [M, K] -> (packed E2M1 [M, K/2] u8, blocked E8M0 scales)."""
+    return _quant(_lib.mxfp4_quantize, 32, A, Aq, A_sf, stream, "mxfp4_quantize")
+
+
+def nvfp4_quantize(A, Aq=None, A_sf=None, stream=None):
+    """bf16 A [M, K] -> (packed E2M1 [M, K/2] u8, blocked E4M3 scales)."""
+    return _quant(_lib.nvfp4_quantize, 16, A, Aq, A_sf, stream, "nvfp4_quantize")
+
+
+# ------------------------------------------------------------------ GEMM --
+
+def mxfp4_gemm_a4w4(Aq, A_sf, Bq, B_sf, K: int, C=None, workspace=None, stream=None):
+    """C [M, N] bf16 = (Aq, A_sf) x (Bq, B_sf)^T."""
+    _dev(Aq, "Aq", torch.uint8, 2)
+    _dev(Bq, "Bq", torch.uint8, 2)
+    M, N = Aq.shape[0], Bq.shape[0]
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=Aq.device)
+    if workspace is None:
+        workspace = new_workspace(M, N, K, Aq.device)
+    _dev(C, "C", torch.bfloat16, 2)
+    _check(_lib.mxfp4_gemm_a4w4(Aq.data_ptr(), Aq.stride(0), A_sf.data_ptr(), Bq.data_ptr(),
+                                Bq.stride(0), B_sf.data_ptr(), C.data_ptr(), C.stride(0), M, N, K,
+                                workspace.data_ptr(), workspace.numel(), _stream_ptr(stream)),
+           "mxfp4_gemm_a4w4")
+    return C
+
+
+def mxfp4_quant_gemm_fused(A, Bq, B_sf, C=None, workspace=None, stream=None):
+    """C [M, N] bf16 = MXFP4(A) x (Bq, B_sf)^T, quantization fused into the GEMM."""
+    _dev(A, "A", torch.bfloat16, 2)
+    _dev(Bq, "Bq", torch.uint8, 2)
+    M, K = A.shape
+    N = Bq.shape[0]
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    if workspace is None:
+        workspace = new_workspace(M, N, K, A.device)
+    _dev(C, "C", torch.bfloat16, 2)
+    _check(_lib.mxfp4_quant_gemm_fused(A.data_ptr(), A.stride(0), Bq.data_ptr(), Bq.stride(0),
+                                       B_sf.data_ptr(), C.data_ptr(), C.stride(0), M, N, K,
+                                       workspace.data_ptr(), workspace.numel(), _stream_ptr(stream)),
+           "mxfp4_quant_gemm_fused")
+    return C
+
+
+def make_nv_problems(groups):
+    """ctypes array of nvfp4_problem_t from dicts with keys a, sfa, b, sfb, c, k."""
+    arr = (NvProblem * len(groups))()
+    for i, g in enumerate(groups):
+        a, b, c = g["a"], g["b"], g["c"]
+        for name, t in (("a", a), ("b", b), ("c", c), ("sfa", g["sfa"]), ("sfb", g["sfb"])):
+            _dev(t, name)
+        arr[i] = NvProblem(a.shape[0], b.shape[0], g["k"], a.data_ptr(), g["sfa"].data_ptr(),
+                           b.data_ptr(), g["sfb"].data_ptr(), c.data_ptr(),
+                           a.stride(0), b.stride(0), c.stride(0))
+    return arr
+
+
+def nvfp4_group_gemm(groups, problems=None, stream=None):
+    """Grouped NVFP4 GEMM over `groups` (see make_nv_problems); returns the C list."""
+    if problems is None:
+        problems = make_nv_problems(groups)
+    _check(_lib.nvfp4_group_gemm(problems, len(problems), None, 0, _stream_ptr(stream)),
+           "nvfp4_group_gemm")
+    return [g["c"] for g in groups]
+
+
+def get_device_error() -> int:
+    code = ctypes.c_int(0)
+    _check(_lib.mxfp4_get_device_error(ctypes.byref(code)), "mxfp4_get_device_error")
+    return code.value

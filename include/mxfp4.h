@@ -1,0 +1,189 @@
+/*
+ * mxfp4.h -- C ABI of libmxfp4: block-scaled FP4 (MXFP4 / NVFP4) quantization
+ * and GEMM on GB300 (sm_103a).
+ *
+ * Sources of the operations (web pages, by title):
+ *   [MM-517169] kernelbot-amd-mxfp4-mm-517169 -- bf16 A is quantized per 1x32
+ *               block to MXFP4 and multiplied with a pre-quantized MXFP4 weight
+ *               B into bf16 C; its "Optimization 5" docstring motivates the fused
+ *               path in which the quantized A never reaches global memory.
+ *   [MM-683203] kernelbot-amd-mxfp4-mm-683203 -- the quant kernel writes scales
+ *               straight into the layout the GEMM consumes; per-shape state is
+ *               resolved once and the hot path allocates nothing.
+ *   [NV-496271] kernelbot-nvfp4-group-gemm-496271 -- a list of (a, b, c) NVFP4
+ *               problems with E4M3 scales per 16 elements in the 128x4 blocked
+ *               layout, each multiplied into an fp16 C.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Pointers named A, Aq, B, Bq, C, *_sf and workspace are DEVICE pointers
+ *   (memory of the current CUDA device). `problems` in nvfp4_group_gemm is a
+ *   HOST array. The caller owns all memory; the library never allocates or
+ *   frees device memory and never synchronizes the stream.
+ * - `stream` is a cudaStream_t passed as void*; NULL means the legacy default
+ *   stream. Work is enqueued on it asynchronously.
+ * - Matrices are row-major. A leading dimension is given in ELEMENTS for bf16
+ *   and fp16 matrices and in BYTES for packed FP4 matrices.
+ * - Packed FP4 (E2M1): two codes per byte, the even-k element in the low nibble
+ *   ([MM-517169] module docstring); code bit 3 is the sign, bits 0-2 index the
+ *   magnitudes {0, 0.5, 1, 1.5, 2, 3, 4, 6}.
+ * - Scale buffers use the 128x4 blocked layout ([NV-496271] _prepare_scale_for_tma):
+ *   scale (r, c) of a logical [R, C] matrix is the byte at
+ *     ((r/128)*ceil(C/4) + c/4)*512 + (r%32)*16 + ((r%128)/32)*4 + c%4,
+ *   and the buffer holds mxfp4_sf_bytes(R, K, vec) bytes. MXFP4 scales are
+ *   E8M0 (2^(b-127)), one per 32 K-elements; NVFP4 scales are E4M3, one per 16.
+ * - Alignment: every device pointer 16-byte aligned; every row stride a
+ *   multiple of 16 bytes. Violations return MXFP4_ERR_MISALIGNED.
+ * - Errors: arguments are checked on the host before anything is enqueued; a
+ *   non-OK status means nothing was launched. A failed launch returns
+ *   MXFP4_ERR_CUDA. There is no fallback path of any kind.
+ * - Thread safety: calls may come from several host threads; the internal
+ *   plan cache is locked.
+ */
+#ifndef MXFP4_GB300_H
+#define MXFP4_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MXFP4_API __attribute__((visibility("default")))
+#else
+#define MXFP4_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MXFP4_OK = 0,
+    MXFP4_ERR_INVALID_ARG = 1,         /* null pointer, non-positive size, bad enum */
+    MXFP4_ERR_UNSUPPORTED_SHAPE = 2,   /* K not a multiple of the scale vector, too many groups */
+    MXFP4_ERR_MISALIGNED = 3,          /* pointer or row stride breaks the 16-byte rule */
+    MXFP4_ERR_WORKSPACE_TOO_SMALL = 4, /* ws_bytes below the matching *_workspace_bytes() */
+    MXFP4_ERR_CUDA = 5,                /* a CUDA runtime/driver call failed */
+    MXFP4_ERR_DEVICE_TIMEOUT = 6,      /* a kernel gave up waiting (see mxfp4_get_device_error) */
+    MXFP4_ERR_NO_DEVICE = 7            /* current device is not a compute capability 10.3 GPU */
+} mxfp4_status_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+MXFP4_API const char *mxfp4_status_string(mxfp4_status_t status);
+
+/* ABI version of this header; bumps on any incompatible change. */
+MXFP4_API int mxfp4_abi_version(void);
+
+/* Bytes of a blocked scale buffer for `rows` rows of `k` FP4 elements with one
+ * scale per `vec` elements (vec = 32 for MXFP4, 16 for NVFP4):
+ * ceil(rows/128) * ceil((k/vec)/4) * 512. Returns 0 if vec is not 16 or 32,
+ * k is not a multiple of vec, or a size is not positive. */
+MXFP4_API size_t mxfp4_sf_bytes(int64_t rows, int64_t k, int vec);
+
+/* ---------------------------------------------------------- quantization -- */
+
+/* Dynamic per-1x32 MXFP4 quantization of bf16 A [M, K] ([MM-517169] module
+ * docstring steps 1-2; [MM-683203] _quant_shuffled writes the scales directly
+ * in the consumer's layout). Per 32-element block along K:
+ *   e = clamp(floor(log2(amax)) - 2, -127, 127), amax = 0 -> e = -127;
+ *   scale byte = e + 127;  code_i = E2M1 round-half-to-even of x_i * 2^-e,
+ *   saturating at +-6, IEEE sign kept (-0 -> 0x8).
+ *   A    : bf16 [M, K], row stride lda elements (lda >= K, lda*2 % 16 == 0).
+ *   Aq   : out, uint8 [M, K/2], row stride ldq bytes (ldq >= K/2, ldq % 16 == 0).
+ *   A_sf : out, blocked E8M0 scales, mxfp4_sf_bytes(M, K, 32) bytes; every pad
+ *          cell is written with 0x7F (scale 1.0, [MM-683203] key trick 2).
+ * K must be a positive multiple of 32. Also used to pre-quantize weights B. */
+MXFP4_API mxfp4_status_t mxfp4_quantize(const void *A, int64_t M, int64_t K, int64_t lda, void *Aq,
+                              int64_t ldq, void *A_sf, void *stream);
+
+/* Per-1x16 NVFP4 quantization of bf16 A [M, K] (the operand format of
+ * [NV-496271]; the pages do not print the producer's rule, this library's
+ * reading is): s = E4M3(round-to-nearest-even, saturating at 448) of
+ * fp32(amax)/6; code_i = E2M1 RNE of fp32(x_i)/s (fp32 division), saturating;
+ * s == 0 gives zero magnitudes with the sign kept. Same argument meaning as
+ * mxfp4_quantize; A_sf holds mxfp4_sf_bytes(M, K, 16) bytes, pad cells 0x00.
+ * K must be a positive multiple of 16. */
+MXFP4_API mxfp4_status_t nvfp4_quantize(const void *A, int64_t M, int64_t K, int64_t lda, void *Aq,
+                              int64_t ldq, void *A_sf, void *stream);
+
+/* ------------------------------------------------------------------ GEMM -- */
+
+/* Workspace bytes needed by mxfp4_gemm_a4w4 and mxfp4_quant_gemm_fused for
+ * this shape (split-K partial sums, tile tickets and, for the two-kernel path,
+ * the quantized A). Depends only on (M, N, K). The workspace must be filled
+ * with zeros before its FIRST use; every successful call leaves it zeroed
+ * again, so it can be reused for any later call without clearing. Calls that
+ * share one workspace must not run concurrently. */
+MXFP4_API size_t mxfp4_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/* Block-scaled MXFP4 GEMM, C = (Aq * A_sf) x (Bq * B_sf)^T ([MM-517169]
+ * docstring steps 3-4 and the gemm_a4w4 call; [MM-683203] launch 2): for every
+ * m < M, n < N,
+ *   C[m, n] = bf16_rne( sum_k  e2m1(Aq[m,k]) 2^(A_sf[m,k/32]-127)
+ *                            * e2m1(Bq[n,k]) 2^(B_sf[n,k/32]-127) ),
+ * accumulated in fp32 on the tensor cores (tcgen05.mma kind::mxf4).
+ *   Aq  : uint8 [M, K/2], row stride ldaq bytes;  A_sf: blocked, mxfp4_sf_bytes(M, K, 32).
+ *   Bq  : uint8 [N, K/2], row stride ldbq bytes;  B_sf: blocked, mxfp4_sf_bytes(N, K, 32).
+ *   C   : out, bf16 [M, N], row stride ldc elements (ldc >= N, ldc*2 % 16 == 0).
+ *   workspace: device scratch of ws_bytes >= mxfp4_workspace_bytes(M, N, K).
+ * K must be a positive multiple of 32. */
+MXFP4_API mxfp4_status_t mxfp4_gemm_a4w4(const void *Aq, int64_t ldaq, const void *A_sf, const void *Bq,
+                               int64_t ldbq, const void *B_sf, void *C, int64_t ldc, int64_t M,
+                               int64_t N, int64_t K, void *workspace, size_t ws_bytes,
+                               void *stream);
+
+/* Dynamic MXFP4 quantization of bf16 A fused with the block-scaled GEMM
+ * against pre-quantized Bq ([MM-517169] "Optimization 5"; [MM-683203] docstring).
+ * Result equals mxfp4_quantize(A) followed by mxfp4_gemm_a4w4 (bit-identical
+ * quantization, same accumulation contract). For small M (the activation
+ * rows fit one MMA N-tile) the quantized A is formed on chip and never touches
+ * global memory; for larger M the library runs the quant kernel into the
+ * workspace and then the GEMM.
+ *   A   : bf16 [M, K], row stride lda elements.
+ *   Bq, B_sf, C, ldc, workspace: as in mxfp4_gemm_a4w4. */
+MXFP4_API mxfp4_status_t mxfp4_quant_gemm_fused(const void *A, int64_t lda, const void *Bq, int64_t ldbq,
+                                      const void *B_sf, void *C, int64_t ldc, int64_t M,
+                                      int64_t N, int64_t K, void *workspace, size_t ws_bytes,
+                                      void *stream);
+
+/* One problem of a grouped NVFP4 GEMM ([NV-496271] custom_kernel: each entry of
+ * the problem list carries a, b, c, their scales and (m, n, k)). */
+typedef struct {
+    int64_t m, n, k;   /* C is [m, n]; k is the reduction length (multiple of 16) */
+    const void *a;     /* uint8 [m, k/2] packed E2M1, row stride lda bytes */
+    const void *sfa;   /* blocked E4M3 scales, mxfp4_sf_bytes(m, k, 16) bytes */
+    const void *b;     /* uint8 [n, k/2] packed E2M1, row stride ldb bytes */
+    const void *sfb;   /* blocked E4M3 scales, mxfp4_sf_bytes(n, k, 16) bytes */
+    void *c;           /* out: fp16 [m, n], row stride ldc elements */
+    int64_t lda, ldb, ldc;
+} nvfp4_problem_t;
+
+/* Maximum number of problems in one nvfp4_group_gemm call. */
+#define NVFP4_MAX_GROUPS 16
+
+/* Workspace bytes for nvfp4_group_gemm (currently 0: the grouped kernel keeps
+ * its problem table in kernel parameters). */
+MXFP4_API size_t nvfp4_group_workspace_bytes(int num_groups);
+
+/* Grouped NVFP4 GEMM: for each problem g,
+ *   C_g[m, n] = fp16_rne( sum_k e2m1(a[m,k]) e4m3(sfa[m,k/16]) e2m1(b[n,k]) e4m3(sfb[n,k/16]) )
+ * with fp32 accumulation (tcgen05.mma kind::mxf4nvf4, scale_vec::4X), all
+ * groups in ONE launch scheduled tile by tile ([NV-496271] custom_kernel runs one
+ * launch per group and batch index; a batch index l is flattened into extra
+ * problems by the caller). `problems` is a host array of num_groups entries
+ * (1 <= num_groups <= NVFP4_MAX_GROUPS); it is read during the call only. */
+MXFP4_API mxfp4_status_t nvfp4_group_gemm(const nvfp4_problem_t *problems, int num_groups, void *workspace,
+                                size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------ diagnostics -- */
+
+/* Reads and clears the library's device-side error word. Kernels never trap:
+ * a wait that exceeds its time limit (about 2 s) records a nonzero code there
+ * and the kernel exits cleanly. This call synchronizes the current device.
+ * *code receives 0 when no kernel reported an error. */
+MXFP4_API mxfp4_status_t mxfp4_get_device_error(int *code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP4_GB300_H */

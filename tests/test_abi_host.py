@@ -1,0 +1,102 @@
+"""The C-ABI library builds, loads and exports every declared entry point; host
+logic (sizes, argument validation) works without a GPU. No compute calls."""
+import ctypes
+
+import pytest
+
+from block_scaled_fp4_mxfp4_gb300 import build as libbuild
+
+libbuild.build()
+from block_scaled_fp4_mxfp4_gb300 import mxfp4  # noqa: E402
+
+L = mxfp4.lib()
+
+
+def test_every_declared_symbol_is_exported():
+    names = mxfp4.declared_symbols()
+    assert len(names) == 11
+    for n in names:
+        assert hasattr(L, n), n  # ctypes resolves the exported symbol
+
+
+def test_status_strings_and_version():
+    for code, name in mxfp4.STATUS.items():
+        assert L.mxfp4_status_string(code).decode() == name
+    assert L.mxfp4_status_string(99).decode() == "MXFP4_UNKNOWN_STATUS"
+    assert L.mxfp4_abi_version() == 1
+
+
+@pytest.mark.parametrize("rows,k,vec,want", [
+    (16, 7168, 32, 1 * 56 * 512),      # decode A: 224 scale columns -> 56 blocks
+    (2112, 7168, 32, 17 * 56 * 512),
+    (128, 256, 16, 4 * 512),           # one NVFP4 256-wide K step = 4 blocks
+    (130, 96, 32, 2 * 1 * 512),        # ragged rows and columns
+    (1, 32, 32, 512),
+    (8, 33, 32, 0), (8, 32, 8, 0), (0, 32, 32, 0),
+])
+def test_sf_bytes(rows, k, vec, want):
+    assert L.mxfp4_sf_bytes(rows, k, vec) == want
+
+
+def test_workspace_bytes_is_a_function_of_shape():
+    a = L.mxfp4_workspace_bytes(16, 2112, 7168)
+    assert a == L.mxfp4_workspace_bytes(16, 2112, 7168) > 16 * 7168 // 2
+    assert L.mxfp4_workspace_bytes(8192, 8192, 8192) >= 8192 * 4096 + 8192 * 256
+    assert L.mxfp4_workspace_bytes(16, 2112, 7000) == 0  # K % 32 != 0
+    assert L.nvfp4_group_workspace_bytes(8) == 0
+
+
+def test_quantize_argument_validation_needs_no_gpu():
+    q = L.mxfp4_quantize
+    assert q(None, 1, 32, 32, 16, 16, 16, None) == 1                 # null A
+    assert q(16, 0, 32, 32, 16, 16, 16, None) == 1                   # M = 0
+    assert q(16, 1, 48, 48, 16, 32, 16, None) == 2                   # K % 32
+    assert q(16, 1, 32, 31, 16, 16, 16, None) == 1                   # lda < K
+    assert q(16, 1, 32, 36, 16, 16, 16, None) == 3                   # lda*2 % 16
+    assert q(24, 1, 32, 32, 16, 16, 16, None) == 3                   # A misaligned
+    assert q(16, 1, 32, 32, 16, 24, 16, None) == 3                   # ldq % 16
+    assert L.nvfp4_quantize(16, 1, 40, 40, 16, 32, 16, None) == 2    # K % 16
+
+
+def test_gemm_argument_validation_needs_no_gpu():
+    g = L.mxfp4_gemm_a4w4
+    ok = dict(Aq=16, ldaq=16, Asf=16, Bq=16, ldbq=16, Bsf=16, C=16, ldc=8, M=1, N=8, K=32, ws=16,
+              wsb=1 << 20, s=None)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return g(a["Aq"], a["ldaq"], a["Asf"], a["Bq"], a["ldbq"], a["Bsf"], a["C"], a["ldc"], a["M"],
+                 a["N"], a["K"], a["ws"], a["wsb"], a["s"])
+
+    assert call(C=None) == 1
+    assert call(K=48) == 2
+    assert call(ldc=4) == 1
+    assert call(ldbq=8) == 1
+    assert call(ws=None) == 1
+    assert call(wsb=0) == 4
+    assert call(Bq=8) == 3
+    f = L.mxfp4_quant_gemm_fused
+    assert f(16, 31, 16, 16, 16, 16, 8, 1, 8, 32, 16, 1 << 20, None) == 1   # lda < K
+    assert f(16, 36, 16, 16, 16, 16, 8, 1, 8, 32, 16, 1 << 20, None) == 3   # lda*2 % 16
+    assert f(16, 32, 16, 16, 16, 16, 8, 1, 8, 32, 16, 0, None) == 4
+
+
+def test_group_gemm_validation_needs_no_gpu():
+    P = mxfp4.NvProblem
+    good = P(64, 128, 256, 16, 16, 16, 16, 16, 128, 128, 128)
+    arr = (P * 1)(good)
+    assert L.nvfp4_group_gemm(None, 1, None, 0, None) == 1
+    assert L.nvfp4_group_gemm(arr, 0, None, 0, None) == 1
+    many = (P * 17)(*([good] * 17))
+    assert L.nvfp4_group_gemm(many, 17, None, 0, None) == 2
+    bad_k = (P * 1)(P(64, 128, 250, 16, 16, 16, 16, 16, 128, 128, 128))
+    assert L.nvfp4_group_gemm(bad_k, 1, None, 0, None) == 2
+    bad_al = (P * 1)(P(64, 128, 256, 24, 16, 16, 16, 16, 128, 128, 128))
+    assert L.nvfp4_group_gemm(bad_al, 1, None, 0, None) == 3
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="checks the no-GPU answer")
+def test_valid_call_without_gpu_reports_no_device():
+    assert L.mxfp4_quantize(16, 1, 32, 32, 16, 16, 16, None) == 7
+    code = ctypes.c_int(-1)
+    assert L.mxfp4_get_device_error(ctypes.byref(code)) == 5

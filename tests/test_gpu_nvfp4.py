@@ -1,0 +1,72 @@
+"""GPU grouped NVFP4 GEMM (tcgen05 kind::mxf4nvf4, E4M3 per 16, fp16 C) vs the
+oracle. Operands are quantized from seeded bf16 on each side (bytes compared
+bit-exactly), then every C_g is checked against the double-precision GEMM."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_scaled_fp4_mxfp4_gb300 import workloads as wl
+from gpu_util import assert_bytes_equal, assert_within_tolerance, c_f64, dev_bf16, host
+
+pytestmark = pytest.mark.gpu
+
+mx = pytest.importorskip("block_scaled_fp4_mxfp4_gb300.mxfp4")
+
+
+def nv_both(bits):
+    q, sf = mx.nvfp4_quantize(dev_bf16(bits))
+    q_ref, sf_ref = oracle.nv_quantize(bits)
+    assert_bytes_equal(host(q), q_ref, "nv codes")
+    assert_bytes_equal(host(sf), sf_ref, "nv scales")
+    return q, sf, q_ref, sf_ref
+
+
+def run_groups(shapes, seed):
+    groups, refs = [], []
+    for i, (m, n, k) in enumerate(shapes):
+        a = wl.gen_bf16(seed, 10 + 2 * i, m, k)
+        b = wl.gen_bf16(seed, 11 + 2 * i, n, k)
+        qa, sfa, qa_r, sfa_r = nv_both(a)
+        qb, sfb, qb_r, sfb_r = nv_both(b)
+        c = torch.full((m, n), float("nan"), dtype=torch.float16, device="cuda")
+        groups.append(dict(a=qa, sfa=sfa, b=qb, sfb=sfb, c=c, k=k))
+        refs.append((qa_r, sfa_r, qb_r, sfb_r, k))
+    mx.nvfp4_group_gemm(groups)
+    torch.cuda.synchronize()
+    for (m, n, k), g, (qa_r, sfa_r, qb_r, sfb_r, _) in zip(shapes, groups, refs):
+        c_ref, s = oracle.gemm_full(qa_r, sfa_r, qb_r, sfb_r, k, 16)
+        assert_within_tolerance(c_f64(g["c"]), c_ref, s, f"nvfp4 group {m}x{n}x{k}")
+    assert mx.get_device_error() == 0
+
+
+def test_single_group_small():
+    run_groups([(128, 256, 256)], 1)
+
+
+def test_groups_ragged_m_n_k():
+    run_groups([(64, 256, 512), (1, 130, 16), (130, 300, 272), (257, 512, 1024), (200, 64, 48)], 2)
+
+
+def test_eight_groups_small_k():
+    shapes = [(m, 512, 256) for m in (64, 128, 256, 384, 512, 640, 768, 1024)]
+    run_groups(shapes, 3)
+
+
+def test_sixteen_groups_max():
+    shapes = [(16 + 8 * i, 128 + 64 * (i % 3), 128 + 32 * (i % 4)) for i in range(16)]
+    run_groups(shapes, 4)
+
+
+def test_probe_single_nonzero():
+    m_, n_, k_ = 130, 260, 512
+    for (m, n, k) in [(0, 0, 0), (129, 259, 511), (40, 140, 17), (3, 200, 300)]:
+        a = np.zeros((m_, k_)); a[m, k] = 1.5
+        b = np.zeros((n_, k_)); b[n, k] = -1.5
+        qa, sfa, _, _ = nv_both(wl.to_bf16_bits(a))
+        qb, sfb, _, _ = nv_both(wl.to_bf16_bits(b))
+        c = torch.zeros((m_, n_), dtype=torch.float16, device="cuda")
+        mx.nvfp4_group_gemm([dict(a=qa, sfa=sfa, b=qb, sfb=sfb, c=c, k=k_)])
+        C = c_f64(c)
+        want = np.zeros((m_, n_)); want[m, n] = -2.25
+        assert np.array_equal(C, want), (m, n, k, np.argwhere(C != want)[:5])
