@@ -129,6 +129,8 @@ mxfp4_status_t fp4_map(const void *base, int64_t inner, int64_t rows, int64_t st
 
 // ------------------------------------------------------------- validation
 inline bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool al4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+inline bool al2(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 1u) == 0; }
 
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 
@@ -139,8 +141,9 @@ mxfp4_status_t check_quant(const void *A, int64_t M, int64_t K, int64_t lda, con
     if (M < 1 || K < 1 || M > kMaxDim || K > kMaxDim) return MXFP4_ERR_INVALID_ARG;
     if (K % vec != 0) return MXFP4_ERR_UNSUPPORTED_SHAPE;
     if (lda < K || ldq < K / 2) return MXFP4_ERR_INVALID_ARG;
-    if ((lda * 2) % 16 != 0 || ldq % 16 != 0) return MXFP4_ERR_MISALIGNED;
-    if (!al16(A) || !al16(Aq) || !al16(sf)) return MXFP4_ERR_MISALIGNED;
+    // 16-byte vector loads of A; 4-byte stores of codes and scale words
+    if ((lda * 2) % 16 != 0 || ldq % 4 != 0) return MXFP4_ERR_MISALIGNED;
+    if (!al16(A) || !al4(Aq) || !al4(sf)) return MXFP4_ERR_MISALIGNED;
     return MXFP4_OK;
 }
 
@@ -151,8 +154,9 @@ mxfp4_status_t check_gemm_common(const void *Bq, int64_t ldbq, const void *B_sf,
     if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return MXFP4_ERR_INVALID_ARG;
     if (K % 32 != 0) return MXFP4_ERR_UNSUPPORTED_SHAPE;
     if (ldbq < K / 2 || ldc < N) return MXFP4_ERR_INVALID_ARG;
-    if (ldbq % 16 != 0 || (ldc * 2) % 16 != 0) return MXFP4_ERR_MISALIGNED;
-    if (!al16(Bq) || !al16(B_sf) || !al16(C)) return MXFP4_ERR_MISALIGNED;
+    // TMA operands: 16-byte base and row stride; C needs only element alignment
+    if (ldbq % 16 != 0) return MXFP4_ERR_MISALIGNED;
+    if (!al16(Bq) || !al16(B_sf) || !al2(C)) return MXFP4_ERR_MISALIGNED;
     return MXFP4_OK;
 }
 
@@ -368,8 +372,8 @@ mxfp4_status_t nvfp4_group_gemm(const nvfp4_problem_t *problems, int num_groups,
             return MXFP4_ERR_INVALID_ARG;
         if (p.k % 16 != 0) return MXFP4_ERR_UNSUPPORTED_SHAPE;
         if (p.lda < p.k / 2 || p.ldb < p.k / 2 || p.ldc < p.n) return MXFP4_ERR_INVALID_ARG;
-        if (p.lda % 16 != 0 || p.ldb % 16 != 0 || (p.ldc * 2) % 16 != 0) return MXFP4_ERR_MISALIGNED;
-        if (!al16(p.a) || !al16(p.sfa) || !al16(p.b) || !al16(p.sfb) || !al16(p.c)) return MXFP4_ERR_MISALIGNED;
+        if (p.lda % 16 != 0 || p.ldb % 16 != 0) return MXFP4_ERR_MISALIGNED;
+        if (!al16(p.a) || !al16(p.sfa) || !al16(p.b) || !al16(p.sfb) || !al2(p.c)) return MXFP4_ERR_MISALIGNED;
         total_tiles += ((p.m + 127) / 128) * ((p.n + bn - 1) / bn);
     }
     if (total_tiles > kMaxDim) return MXFP4_ERR_UNSUPPORTED_SHAPE;

@@ -90,7 +90,7 @@ __device__ __forceinline__ void store_row32(void *c, int64_t ldc, int row, int c
 {
     if constexpr (F16) {
         __half *p = static_cast<__half *>(c) + static_cast<int64_t>(row) * ldc + col0;
-        if (col0 + 32 <= n) {
+        if (col0 + 32 <= n && (reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 uint4 w;
@@ -111,7 +111,7 @@ __device__ __forceinline__ void store_row32(void *c, int64_t ldc, int row, int c
         }
     } else {
         __nv_bfloat16 *p = static_cast<__nv_bfloat16 *>(c) + static_cast<int64_t>(row) * ldc + col0;
-        if (col0 + 32 <= n) {
+        if (col0 + 32 <= n && (reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 uint4 w;

@@ -131,7 +131,9 @@ def _quant(fn, vec, A, Aq, A_sf, stream, where):
     _dev(A, "A", torch.bfloat16, 2)
     M, K = A.shape
     if Aq is None:
-        Aq = torch.empty((M, K // 2), dtype=torch.uint8, device=A.device)
+        # row stride rounded up to 16 bytes so Aq can feed the TMA-based GEMMs
+        ld = (K // 2 + 15) // 16 * 16
+        Aq = torch.empty((M, ld), dtype=torch.uint8, device=A.device)[:, :K // 2]
     if A_sf is None:
         A_sf = torch.empty(max(1, sf_bytes(M, K, vec)), dtype=torch.uint8, device=A.device)
     _dev(Aq, "Aq", torch.uint8, 2)

@@ -32,8 +32,12 @@
  *     ((r/128)*ceil(C/4) + c/4)*512 + (r%32)*16 + ((r%128)/32)*4 + c%4,
  *   and the buffer holds mxfp4_sf_bytes(R, K, vec) bytes. MXFP4 scales are
  *   E8M0 (2^(b-127)), one per 32 K-elements; NVFP4 scales are E4M3, one per 16.
- * - Alignment: every device pointer 16-byte aligned; every row stride a
- *   multiple of 16 bytes. Violations return MXFP4_ERR_MISALIGNED.
+ * - Alignment (violations return MXFP4_ERR_MISALIGNED): bf16 inputs A are
+ *   read with 16-byte vectors (A 16-byte aligned, lda a multiple of 8);
+ *   packed FP4 GEMM operands and every scale buffer a GEMM reads are loaded
+ *   by TMA (16-byte aligned, packed row stride a multiple of 16 bytes);
+ *   quantizer outputs need 4-byte alignment (ldq a multiple of 4); C needs
+ *   only element alignment.
  * - Errors: arguments are checked on the host before anything is enqueued; a
  *   non-OK status means nothing was launched. A failed launch returns
  *   MXFP4_ERR_CUDA. There is no fallback path of any kind.
@@ -87,8 +91,9 @@ MXFP4_API size_t mxfp4_sf_bytes(int64_t rows, int64_t k, int vec);
  *   e = clamp(floor(log2(amax)) - 2, -127, 127), amax = 0 -> e = -127;
  *   scale byte = e + 127;  code_i = E2M1 round-half-to-even of x_i * 2^-e,
  *   saturating at +-6, IEEE sign kept (-0 -> 0x8).
- *   A    : bf16 [M, K], row stride lda elements (lda >= K, lda*2 % 16 == 0).
- *   Aq   : out, uint8 [M, K/2], row stride ldq bytes (ldq >= K/2, ldq % 16 == 0).
+ *   A    : bf16 [M, K], row stride lda elements (lda >= K, lda % 8 == 0).
+ *   Aq   : out, uint8 [M, K/2], row stride ldq bytes (ldq >= K/2, ldq % 4 == 0;
+ *          a multiple of 16 if Aq is later a GEMM operand).
  *   A_sf : out, blocked E8M0 scales, mxfp4_sf_bytes(M, K, 32) bytes; every pad
  *          cell is written with 0x7F (scale 1.0, [MM-683203] key trick 2).
  * K must be a positive multiple of 32. Also used to pre-quantize weights B. */
@@ -110,9 +115,10 @@ MXFP4_API mxfp4_status_t nvfp4_quantize(const void *A, int64_t M, int64_t K, int
 /* Workspace bytes needed by mxfp4_gemm_a4w4 and mxfp4_quant_gemm_fused for
  * this shape (split-K partial sums, tile tickets and, for the two-kernel path,
  * the quantized A). Depends only on (M, N, K). The workspace must be filled
- * with zeros before its FIRST use; every successful call leaves it zeroed
- * again, so it can be reused for any later call without clearing. Calls that
- * share one workspace must not run concurrently. */
+ * with zeros before its FIRST use; every successful call leaves the counters
+ * inside it at zero again (the rest is scratch), so it can be reused for any
+ * later call without clearing. Calls that share one workspace must not run
+ * concurrently. */
 MXFP4_API size_t mxfp4_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /* Block-scaled MXFP4 GEMM, C = (Aq * A_sf) x (Bq * B_sf)^T ([MM-517169]
@@ -123,7 +129,7 @@ MXFP4_API size_t mxfp4_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * accumulated in fp32 on the tensor cores (tcgen05.mma kind::mxf4).
  *   Aq  : uint8 [M, K/2], row stride ldaq bytes;  A_sf: blocked, mxfp4_sf_bytes(M, K, 32).
  *   Bq  : uint8 [N, K/2], row stride ldbq bytes;  B_sf: blocked, mxfp4_sf_bytes(N, K, 32).
- *   C   : out, bf16 [M, N], row stride ldc elements (ldc >= N, ldc*2 % 16 == 0).
+ *   C   : out, bf16 [M, N], row stride ldc elements (ldc >= N).
  *   workspace: device scratch of ws_bytes >= mxfp4_workspace_bytes(M, N, K).
  * K must be a positive multiple of 32. */
 MXFP4_API mxfp4_status_t mxfp4_gemm_a4w4(const void *Aq, int64_t ldaq, const void *A_sf, const void *Bq,

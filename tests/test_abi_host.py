@@ -54,7 +54,7 @@ def test_quantize_argument_validation_needs_no_gpu():
     assert q(16, 1, 32, 31, 16, 16, 16, None) == 1                   # lda < K
     assert q(16, 1, 32, 36, 16, 16, 16, None) == 3                   # lda*2 % 16
     assert q(24, 1, 32, 32, 16, 16, 16, None) == 3                   # A misaligned
-    assert q(16, 1, 32, 32, 16, 24, 16, None) == 3                   # ldq % 16
+    assert q(16, 1, 32, 32, 16, 18, 16, None) == 3                   # ldq % 4
     assert L.nvfp4_quantize(16, 1, 40, 40, 16, 32, 16, None) == 2    # K % 16
 
 
