@@ -1,0 +1,536 @@
+#!/usr/bin/env python
+"""Benchmark of the block-scaled FP4 hot path on GB300.
+
+A step is one call of the hot path on one batch of synthetic input:
+  decode (default)  mxfp4_quant_gemm_fused, A bf16 [16, 7168] x MXFP4 B [2112, 7168]
+  tiny / medium / compute   the other MXFP4 quant+GEMM shapes
+  nvfp4_grouped     nvfp4_group_gemm over 8 groups (M_g 64..1024, N 4096, K 7168)
+Weights are pre-quantized once, untimed, by the library's own quantizer.
+
+Prints one JSON line (rank 0). `value` is microseconds per call over the whole
+job (all ranks), lower is better. The timed region holds exactly --steps steps
+between a barrier + synchronize on both sides; HBM-bound shapes rotate over
+enough copies of their inputs to exceed twice the L2 size. The timed steps are
+replayed from CUDA graphs so host launch cost does not pad the timing.
+
+--impl reference times the CPU oracle (the pages' method restated in plain C,
+fp64) on a bounded sample of the same workload, scaled to one full call.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from block_scaled_fp4_mxfp4_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "µs/call & TFLOP/s, MXFP4 quant+GEMM; % of FP4-tensor/HBM roofline (1 GB300)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor ratio
+
+WORKLOADS = {
+    "decode": wl.DECODE,
+    "tiny": wl.TINY,
+    "medium": wl.MEDIUM,
+    "compute": wl.COMPUTE,
+    "nvfp4_grouped": wl.NVFP4_GROUPED,
+}
+DEFAULT_STEPS = {"decode": 20000, "tiny": 20000, "medium": 10000, "compute": 50, "nvfp4_grouped": 500}
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=None)
+    p.add_argument("--warmup", type=int, default=None)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "block_scaled_fp4_mxfp4_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload, kernel_files):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary table, or None if that kernel's source changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash(kernel_files)
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload and parts[1] == want:
+                return int(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = ""
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5], f[6], f[7], f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        top = max(r[0] for r in rows)
+        loaded = [r for r in rows if r[0] >= 0.5 * top] or rows
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in loaded:
+            for name, v in zip(names, r[2:]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(loaded)}
+
+
+# ----------------------------------------------------------------- GPU arm --
+
+class MXCase:
+    """One MXFP4 quant+GEMM workload resident on the device, with L2 rotation."""
+
+    def __init__(self, w, dev, mx, torch):
+        self.w, self.mx, self.torch = w, mx, torch
+        a_bits, b_bits = wl.gen_a(w), wl.gen_b(w)
+        to = lambda bits: torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        A0 = to(a_bits)
+        Bq0, Bsf0 = mx.mxfp4_quantize(to(b_bits))   # weight pre-quantization (untimed)
+        torch.cuda.synchronize()
+        self.a_host_bits = a_bits
+        per = A0.numel() * 2 + Bq0.numel() + Bsf0.numel() + w.M * w.N * 2
+        l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20)
+        self.rot = max(1, min(64, math.ceil(2 * l2 / per)))
+        self.A = [A0] + [A0.clone() for _ in range(self.rot - 1)]
+        self.Bq = [Bq0.contiguous()] + [Bq0.contiguous().clone() for _ in range(self.rot - 1)]
+        self.Bsf = [Bsf0] + [Bsf0.clone() for _ in range(self.rot - 1)]
+        self.C = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
+        self.ws = mx.new_workspace(w.M, w.N, w.K, dev)
+        self.fused = w.M <= 64      # the library's fused small-M path (one launch)
+        self.launches_per_step = 1 if self.fused else 2
+        self.kernel_files = ["fused.cu", "ptx.cuh", "quant_math.cuh"] if self.fused else ["gemm.cu", "ptx.cuh"]
+        self.rot_bytes = per * self.rot
+
+    def step(self, i):
+        j = i % self.rot
+        self.mx.mxfp4_quant_gemm_fused(self.A[j], self.Bq[j], self.Bsf[j], self.C, self.ws)
+
+    def prepare_gemm_only(self):
+        """Pre-quantized A for timing the GEMM kernel of the two-kernel path alone."""
+        self._aq, self._asf = self.mx.mxfp4_quantize(self.A[0])
+
+    def step_gemm_only(self, i):
+        j = i % self.rot
+        self.mx.mxfp4_gemm_a4w4(self._aq, self._asf, self.Bq[j], self.Bsf[j], self.w.K, self.C, self.ws)
+
+    def alg_bytes(self):
+        return self.w.alg_bytes
+
+    def gemm_alg_bytes(self):
+        """Bytes the GEMM kernel of the two-kernel path must move: packed A and B,
+        both scale sets and bf16 C."""
+        w = self.w
+        return w.M * w.K // 2 + w.M * w.K // 32 + w.N * w.K // 2 + w.N * w.K // 32 + 2 * w.M * w.N
+
+    def e2e(self, steps, torch):
+        """Host buffers: per step copy A in from pinned memory, call, copy C out."""
+        w = self.w
+        a_pin = torch.from_numpy(self.a_host_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+        c_pin = torch.empty((w.M, w.N), dtype=torch.bfloat16).pin_memory()
+        A_dev = torch.empty_like(self.A[0])
+        s = torch.cuda.current_stream()
+
+        def one(i):
+            A_dev.copy_(a_pin, non_blocking=True)
+            self.mx.mxfp4_quant_gemm_fused(A_dev, self.Bq[i % self.rot], self.Bsf[i % self.rot], self.C, self.ws)
+            c_pin.copy_(self.C, non_blocking=True)
+
+        for i in range(3):
+            one(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for i in range(steps):
+            one(i)
+        e1.record(s)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1000.0 / steps, a_pin.numel() * 2, c_pin.numel() * 2
+
+
+class NVCase:
+    """Grouped NVFP4 workload: operands quantized once (untimed) by nvfp4_quantize."""
+
+    def __init__(self, w, dev, mx, torch):
+        self.w, self.mx, self.torch = w, mx, torch
+        to = lambda bits: torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        self.groups = []
+        for g in range(len(w.Ms)):
+            a_bits, b_bits = wl.gen_nv_group(w, g)
+            qa, sfa = mx.nvfp4_quantize(to(a_bits))
+            qb, sfb = mx.nvfp4_quantize(to(b_bits))
+            c = torch.empty((w.Ms[g], w.N), dtype=torch.float16, device=dev)
+            self.groups.append(dict(a=qa, sfa=sfa, b=qb, sfb=sfb, c=c, k=w.K))
+        torch.cuda.synchronize()
+        self.problems = mx.make_nv_problems(self.groups)
+        self.rot = 1                # 178 MB of operands per call already exceed twice the L2
+        self.launches_per_step = 1
+        self.kernel_files = ["gemm.cu", "ptx.cuh"]
+        self.rot_bytes = w.alg_bytes
+
+    def step(self, i):
+        self.mx.nvfp4_group_gemm(self.groups, self.problems)
+
+    def alg_bytes(self):
+        return self.w.alg_bytes
+
+    def e2e(self, steps, torch):
+        """Host buffers: per step copy every A_g (+ scales) in, call, copy every C_g out."""
+        pins_in = [(g["a"].cpu().pin_memory(), g["sfa"].cpu().pin_memory()) for g in self.groups]
+        pins_out = [torch.empty_like(g["c"], device="cpu").pin_memory() for g in self.groups]
+        s = torch.cuda.current_stream()
+
+        def one():
+            for (pa, ps), g in zip(pins_in, self.groups):
+                g["a"].copy_(pa, non_blocking=True)
+                g["sfa"].copy_(ps, non_blocking=True)
+            self.mx.nvfp4_group_gemm(self.groups, self.problems)
+            for po, g in zip(pins_out, self.groups):
+                po.copy_(g["c"], non_blocking=True)
+
+        for _ in range(2):
+            one()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(steps):
+            one()
+        e1.record(s)
+        torch.cuda.synchronize()
+        h2d = sum(pa.numel() + ps.numel() for pa, ps in pins_in)
+        d2h = sum(po.numel() * 2 for po in pins_out)
+        return e0.elapsed_time(e1) * 1000.0 / steps, h2d, d2h
+
+
+def run_ours(args, name, rank, world, local_rank):
+    import torch
+    from block_scaled_fp4_mxfp4_gb300 import mxfp4 as mx
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[name]
+    steps = args.steps if args.steps is not None else DEFAULT_STEPS[name]
+    warmup = args.warmup if args.warmup is not None else max(3, min(100, steps // 10))
+    case = NVCase(w, dev, mx, torch) if name == "nvfp4_grouped" else MXCase(w, dev, mx, torch)
+
+    for i in range(max(warmup, case.rot)):  # warm-up (also encodes every TMA descriptor once)
+        case.step(i)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    cap_stream = torch.cuda.Stream()
+
+    def capture(fn, count):
+        """CUDA graphs holding exactly `count` calls of fn(i), in chunks of G."""
+        G = case.rot * max(1, min(1000, count) // case.rot)
+        graphs = []
+        for c in ([G] * (count // G)) + ([count % G] if count % G else []):
+            if graphs and c == graphs[0][1]:
+                graphs.append(graphs[0])     # replay the same chunk again
+                continue
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap_stream):
+                for i in range(c):
+                    fn(i)
+            graphs.append((g, c))
+        return graphs
+
+    def timed(graphs, settle_s):
+        s = torch.cuda.current_stream()
+        t_end = time.time() + settle_s      # untimed replays so clocks settle
+        while time.time() < t_end:
+            graphs[0][0].replay()
+            torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for g, _ in graphs:
+            g.replay()
+        e1.record(s)
+        barrier()
+        return e0.elapsed_time(e1)
+
+    step_graphs = capture(case.step, steps)
+    with ClockSampler(local_rank) as clk:
+        elapsed_ms = timed(step_graphs, 0.5)
+    del step_graphs
+    kernel_timing = "per step (one launch per step)"
+    per_kernel_us = elapsed_ms * 1000.0 / steps
+    split_times = None
+    if case.launches_per_step > 1:
+        # the dominant kernel (the GEMM) timed alone on the same rotation
+        case.prepare_gemm_only()
+        gemm_graphs = capture(case.step_gemm_only, steps)
+        gemm_ms = timed(gemm_graphs, 0.1)
+        del gemm_graphs
+        per_kernel_us = gemm_ms * 1000.0 / steps
+        split_times = {"gemm_us": per_kernel_us, "step_us": elapsed_ms * 1000.0 / steps}
+        kernel_timing = "GEMM kernel timed alone: CUDA-graph replay of --steps launches"
+
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    elapsed_ms = float(t.item())
+
+    us_per_call = elapsed_ms * 1000.0 / (steps * world)
+    tflops = w.flops * steps * world / (elapsed_ms * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    clocks = clk.summary()
+
+    # roofline of the dominant kernel
+    if name == "compute":
+        fp4_peak = peaks["bf16_tflops_sustained"] * FP4_OVER_BF16
+        ach = w.flops / (per_kernel_us * 1e-6) / 1e12
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
+                "frac": round(ach / fp4_peak, 4),
+                "peak_source": f"{peak_src} bf16 sustained x {FP4_OVER_BF16:g} (nominal FP4:BF16)"}
+        kname = "bs_gemm_kernel<mxf4>"
+    else:
+        if name == "medium":
+            nbytes = case.gemm_alg_bytes()
+            kname = "bs_gemm_kernel<mxf4>"
+        else:
+            nbytes = case.alg_bytes()
+            kname = "fused_quant_gemm_kernel" if name != "nvfp4_grouped" else "bs_gemm_kernel<mxf4nvf4>"
+        ach = nbytes / (per_kernel_us * 1e-6) / 1e9
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm_gbs"], 4), "peak_source": f"{peak_src} hbm_gbs"}
+    roof["traffic"] = ncu_traffic(name, case.kernel_files)
+    roof["kernel"] = kname
+    roof["kernel_us"] = round(per_kernel_us, 3)
+    roof["kernel_timing"] = kernel_timing
+
+    line = {
+        "metric": METRIC, "value": round(us_per_call, 4), "unit": "us/call", "n_gpus": world,
+        "steps": steps, "warmup": warmup, "ms_per_step": round(elapsed_ms / steps, 6),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "fp4 e2m1 (fp32 accumulate)",
+        "data": "synthetic (seeded SplitMix64/Box-Muller; weights pre-quantized untimed)",
+        "config": {"workload": w.name, "parallelism": f"replicas x{world}",
+                   "l2": (f"rotating {case.rot} copies of inputs ({case.rot_bytes / 1e6:.0f} MB > 2x L2)"
+                          if case.rot > 1 else "inputs larger than 2x L2 per call"),
+                   "timing": "CUDA graph replay of the timed steps"},
+        "tflops": round(tflops, 3),
+        "roofline": roof,
+        "gpu_launches": steps * case.launches_per_step,
+        "clocks": clocks,
+    }
+    if split_times:
+        line["kernels_us"] = {k: round(v, 3) for k, v in split_times.items()}
+
+    if not args.no_e2e:
+        short = case.launches_per_step == 1 and name != "nvfp4_grouped"
+        e2e_steps = max(10, min(steps, 2000 if short else 20))
+        e_us, h2d, d2h = case.e2e(e2e_steps, torch)
+        t = torch.tensor([e_us], dtype=torch.float64, device=dev)
+        if world > 1:
+            import torch.distributed as dist
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        line["e2e"] = {"value": round(float(t.item()) / world, 4), "unit": "us/call",
+                       "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(name, budget_s=12.0)
+    return line
+
+
+# ------------------------------------------------------------- oracle arm --
+
+_ORACLE_PREP = {}
+
+
+def _oracle_prep(name):
+    """Untimed oracle-side inputs: bf16 activations and the pre-quantized weights."""
+    import oracle
+    if name in _ORACLE_PREP:
+        return _ORACLE_PREP[name]
+    w = WORKLOADS[name]
+    if name == "nvfp4_grouped":
+        prep = []
+        for g in range(len(w.Ms)):
+            a_bits, b_bits = wl.gen_nv_group(w, g)
+            qb, sfb = oracle.nv_quantize(b_bits)
+            prep.append((a_bits, qb, sfb))
+    else:
+        a_bits = wl.gen_a(w) if w.M <= 4096 else wl.gen_a(w, M=64)
+        qb, sfb = oracle.mx_quantize(wl.gen_b(w))
+        prep = (a_bits, qb, sfb)
+    _ORACLE_PREP[name] = prep
+    return prep
+
+
+def oracle_call_sampled(name, budget_s):
+    """Time the oracle on a bounded sample of one call; return (us per full call, sample text)."""
+    import oracle
+    w = WORKLOADS[name]
+    if name == "nvfp4_grouped":
+        # sample: the first r rows of every group, all N columns
+        prep = _oracle_prep(name)
+        t0 = time.perf_counter()
+        a_bits, qb, sfb = prep[0]
+        qa, sfa = oracle.nv_quantize(a_bits[:1])
+        oracle.gemm_sampled(qa, sfa, qb, sfb, w.K, 16, np.zeros(w.N, np.int64), np.arange(w.N))
+        per_row = time.perf_counter() - t0
+        total_rows = sum(w.Ms)
+        r = max(1, min(max(w.Ms), int(budget_s / per_row / len(w.Ms))))
+        t0 = time.perf_counter()
+        done_rows = 0
+        for a_bits, qb, sfb in prep:
+            rr = min(r, a_bits.shape[0])
+            qa, sfa = oracle.nv_quantize(a_bits[:rr])
+            rows = np.repeat(np.arange(rr), w.N)
+            cols = np.tile(np.arange(w.N), rr)
+            oracle.gemm_sampled(qa, sfa, qb, sfb, w.K, 16, rows, cols)
+            done_rows += rr
+        dt = time.perf_counter() - t0
+        return (dt / done_rows * total_rows * 1e6,
+                f"first {r} rows of each group x all {w.N} columns (quantize + GEMM), scaled by rows")
+    a_bits, qb, sfb = _oracle_prep(name)
+    t0 = time.perf_counter()
+    qa, sfa = oracle.mx_quantize(a_bits[:1])
+    oracle.gemm_sampled(qa, sfa, qb, sfb, w.K, 32, np.zeros(w.N, np.int64), np.arange(w.N))
+    per_row = time.perf_counter() - t0
+    r = max(1, min(w.M, a_bits.shape[0], int(budget_s / per_row)))
+    t0 = time.perf_counter()
+    qa, sfa = oracle.mx_quantize(a_bits[:r])
+    if r == w.M:
+        oracle.gemm_full(qa, sfa, qb, sfb, w.K, 32)
+    else:
+        oracle.gemm_sampled(qa, sfa, qb, sfb, w.K, 32, np.repeat(np.arange(r), w.N), np.tile(np.arange(w.N), r))
+    dt = time.perf_counter() - t0
+    full = "the full call" if r == w.M else f"rows 0..{r - 1} of {w.M} x all {w.N} columns, scaled by rows"
+    return dt / r * w.M * 1e6, f"{full} (quantize A + dequantize-then-fp64 GEMM)"
+
+
+def cpu_baseline(name, budget_s):
+    us, sample = oracle_call_sampled(name, budget_s)
+    return {"value": round(us, 1), "unit": "us/call", "cores": 1, "kind": "oracle", "sample": sample}
+
+
+def run_reference(args, name):
+    w = WORKLOADS[name]
+    steps = args.steps if args.steps is not None else 5
+    warmup = args.warmup if args.warmup is not None else 1
+    budget = max(0.5, min(20.0, 150.0 / (steps + warmup)))
+    for _ in range(warmup):
+        oracle_call_sampled(name, budget)
+    vals = []
+    sample = ""
+    for _ in range(steps):
+        us, sample = oracle_call_sampled(name, budget)
+        vals.append(us)
+    us = statistics.mean(vals)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": "us/call", "n_gpus": 1,
+        "steps": steps, "warmup": warmup, "ms_per_step": round(us / 1000.0, 3), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "parallelism": "single host thread"},
+        "cpu_baseline": {"value": round(us, 1), "unit": "us/call", "cores": 1, "kind": "oracle",
+                         "sample": f"per step: {sample}"},
+        "e2e": {"value": round(us, 1), "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, args.workload)), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    line = run_ours(args, args.workload, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
