@@ -70,11 +70,11 @@ bool encoder()
 struct MapKey {
     uintptr_t ptr;
     int64_t inner, rows, stride;
-    int box_rows, dev;
+    int box_rows, dev, kind;   // kind 0: packed FP4 (u8, 128B swizzle)
     bool operator==(const MapKey &o) const
     {
         return ptr == o.ptr && inner == o.inner && rows == o.rows && stride == o.stride &&
-               box_rows == o.box_rows && dev == o.dev;
+               box_rows == o.box_rows && dev == o.dev && kind == o.kind;
     }
 };
 struct MapKeyHash {
@@ -88,20 +88,16 @@ struct MapKeyHash {
         mix(static_cast<uint64_t>(k.stride));
         mix(static_cast<uint64_t>(k.box_rows));
         mix(static_cast<uint64_t>(k.dev));
+        mix(static_cast<uint64_t>(k.kind));
         return static_cast<size_t>(h);
     }
 };
 std::mutex g_map_mu;
 std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
 
-// Tensor map of a packed FP4 matrix [rows, inner bytes] (row stride `stride`
-// bytes), box {128 bytes, box_rows}, 128-byte swizzle, zero fill out of bounds.
-mxfp4_status_t fp4_map(const void *base, int64_t inner, int64_t rows, int64_t stride, int box_rows,
-                       CUtensorMap *out)
+mxfp4_status_t cached_map(const MapKey &key, const void *base, CUtensorMapDataType dtype, cuuint64_t inner,
+                          cuuint32_t box_inner, CUtensorMapSwizzle swz, CUtensorMap *out)
 {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    MapKey key{reinterpret_cast<uintptr_t>(base), inner, rows, stride, box_rows, dev};
     {
         std::lock_guard<std::mutex> lk(g_map_mu);
         auto it = g_maps.find(key);
@@ -112,19 +108,31 @@ mxfp4_status_t fp4_map(const void *base, int64_t inner, int64_t rows, int64_t st
     }
     if (!encoder()) return MXFP4_ERR_CUDA;
     CUtensorMap tm;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(stride)};
-    cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+    cuuint64_t dims[2] = {inner, static_cast<cuuint64_t>(key.rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(key.stride)};
+    cuuint32_t box[2] = {box_inner, static_cast<cuuint32_t>(key.box_rows)};
     cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = g_encode(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
-                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = g_encode(&tm, dtype, 2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return MXFP4_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_map_mu);
     if (g_maps.size() > 4096) g_maps.clear();
     g_maps.emplace(key, tm);
     *out = tm;
     return MXFP4_OK;
+}
+
+// Tensor map of a packed FP4 matrix [rows, inner bytes] (row stride `stride`
+// bytes), box {128 bytes, box_rows}, 128-byte swizzle, zero fill out of bounds.
+mxfp4_status_t fp4_map(const void *base, int64_t inner, int64_t rows, int64_t stride, int box_rows,
+                       CUtensorMap *out)
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    MapKey key{reinterpret_cast<uintptr_t>(base), inner, rows, stride, box_rows, dev, 0};
+    return cached_map(key, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<cuuint64_t>(inner), 128u,
+                      CU_TENSOR_MAP_SWIZZLE_128B, out);
 }
 
 // ------------------------------------------------------------- validation

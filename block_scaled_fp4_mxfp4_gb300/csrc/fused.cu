@@ -6,21 +6,26 @@
 // Design for a weight-streaming (HBM-bound) shape such as M = 16, N = 2112,
 // K = 7168:
 // * Swap A and B: the weight rows fill the MMA's M = 128, the few activation
-//   rows (padded with zeros to MMA_N = 16/32/64/128) are the MMA's N. The
+//   rows (padded with zeros to MMA_N = 16/32/64) are the MMA's N. The
 //   accumulator is D[n][m] = C^T, 128 TMEM lanes x MMA_N columns.
 // * Grid = (ceil(N/128) weight tiles) x (S K-splits); the S CTAs of one weight
 //   tile form a thread-block cluster. Each CTA streams its K-slice of 128
 //   weight rows through a 4-slot TMA ring (evict-first: weights are read once).
-// * Meanwhile warps 2-5 load the CTA's K-slice of bf16 A (every row, 16-byte
-//   vector loads), compute the OCP MX scale per 32-block and the E2M1 codes
-//   with the same arithmetic as the standalone quant kernel, and write them
+// * Warps 2-5 read the CTA's K-slice of bf16 A straight from global memory,
+//   all of a batch's loads in flight at once. A thread owns whole 32-element
+//   blocks (row m, block j): it forms the OCP MX scale and the 32 E2M1 codes
+//   with the same arithmetic as the standalone quant kernel and writes them
 //   into shared memory directly in the MMA's 128-byte-swizzled K-major operand
-//   layout, plus the scales in the 512-byte blocked layout.
+//   layout (16 bytes per block), plus the scale in the 512-byte blocked layout.
+//   Each K-stage is released to the MMA issuer as soon as it is written.
 // * Warp 1 lane 0 copies both operands' scales to TMEM and issues the MMAs.
-// * Split-K reduction without global scratch: every CTA leaves its fp32 tile
-//   in its own shared memory; after a cluster barrier each CTA sums a 1/S slice
-//   of the tile over the S CTAs in rank order (distributed shared memory) and
-//   writes bf16 C. The sum order is fixed, so results are deterministic.
+// * Split-K reduction without global scratch: every CTA pushes the slice of
+//   its fp32 tile that CTA r of the cluster owns (weight rows r*128/S ..) into
+//   r's shared memory with remote stores; after one cluster barrier each CTA
+//   sums its slice over the S sources in rank order and writes bf16 C. The
+//   sum order is fixed, so results are deterministic.
+// Shared memory stays near 100 KB (MMA_N = 16) so two CTAs fit on an SM and
+// every cluster of the grid can be resident at once.
 #include <cstring>
 
 #include "internal.h"
@@ -37,7 +42,9 @@ constexpr int kRing = 4;
 constexpr uint32_t kWBytes = 128 * 128;   // one stage of 128 weight rows x 256 FP4
 constexpr uint32_t kWSfBytes = 2 * 512;   // its two 512-byte scale blocks
 constexpr int kThreads = 192;
-constexpr int kMaxSplits = 16;
+constexpr int kQuantThreads = 128;        // warps 2-5
+constexpr int kMaxSplits = 8;             // portable cluster size
+constexpr int kBatch = 4;                 // 32-element blocks a quant thread keeps in flight
 
 __host__ __device__ constexpr uint32_t pow2_cols_f(uint32_t n)
 {
@@ -46,23 +53,29 @@ __host__ __device__ constexpr uint32_t pow2_cols_f(uint32_t n)
 
 template <int MMA_N>
 struct FusedCfg {
-    static constexpr int MAX_ST = MMA_N <= 64 ? 8 : 4;   // K stages held per CTA
-    static constexpr uint32_t ACT_TILE = MMA_N * 128;     // bytes of one swizzled stage
+    // K stages (256 wide) held per CTA: each has its own quantized operand tile.
+    static constexpr int MAX_ST = MMA_N <= 16 ? 8 : 4;
+    static constexpr int UPS = MMA_N * 8 / kQuantThreads;  // blocks per quant thread per stage
+    static constexpr uint32_t ACT_TILE = MMA_N * 128;      // quantized operand bytes per stage
     static constexpr uint32_t RING_DATA = kRing * kWBytes;
-    static constexpr uint32_t RING_SF = kRing * kWSfBytes;
-    static constexpr uint32_t ACT_DATA = MAX_ST * ACT_TILE;
-    static constexpr uint32_t ACT_SF = MAX_ST * 1024;
-    static constexpr uint32_t BAR_OFF = RING_DATA + RING_SF + ACT_DATA + ACT_SF;
+    static constexpr uint32_t ACT_OFF = RING_DATA;
+    static constexpr uint32_t WSF_OFF = ACT_OFF + MAX_ST * ACT_TILE;
+    static constexpr uint32_t ASF_OFF = WSF_OFF + kRing * kWSfBytes;
+    static constexpr uint32_t RECV_OFF = ASF_OFF + MAX_ST * 1024;
+    // [source rank][m][owned rows] fp32; owned rows = ceil(128 / S) <= 128 / S + 1
+    static constexpr uint32_t RECV_BYTES = MMA_N * (128 + kMaxSplits) * 4;
+    static constexpr uint32_t BAR_OFF = RECV_OFF + RECV_BYTES;
     static constexpr uint32_t SMEM_BYTES = BAR_OFF + 256 + 1024;
-    static constexpr uint32_t SF_COLS = 16;                // 8 weight + 8 activation per slot
+    static constexpr uint32_t SF_COLS = 16;                 // 8 weight + 8 activation per slot
     static constexpr uint32_t TMEM_COLS = pow2_cols_f(MMA_N + kRing * SF_COLS);
+    static_assert(UPS >= 1 && kBatch % UPS == 0, "quant work split");
     static_assert(ACT_TILE % 1024 == 0, "swizzled operand tiles need 1024-byte alignment");
-    static_assert(RING_DATA >= MMA_N * 128 * 4, "reduction tile reuses the weight ring");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert((2 * kRing + MAX_ST + 1) * 8 + 8 <= 256, "barrier area");
 };
 
 struct FusedArgs {
-    const uint16_t *A;
+    const uint16_t *A;    // bf16 [M, K], row stride lda elements
     int64_t lda;
     const uint8_t *sfw;   // weight scales, blocked [N, K/32]
     __nv_bfloat16 *C;
@@ -73,21 +86,22 @@ struct FusedArgs {
 };
 
 template <int MMA_N>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     fused_quant_gemm_kernel(const __grid_constant__ CUtensorMap tmw, const FusedArgs p)
 {
     using Cfg = FusedCfg<MMA_N>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *ring = smem;
-    uint8_t *ring_sf = smem + Cfg::RING_DATA;
-    uint8_t *act = ring_sf + Cfg::RING_SF;
-    uint8_t *act_sf = act + Cfg::ACT_DATA;
+    uint8_t *act = smem + Cfg::ACT_OFF;       // [stage][MMA_N rows x 128 B], 128B-swizzled
+    uint8_t *ring_sf = smem + Cfg::WSF_OFF;   // [slot][2 x 512 B]
+    uint8_t *act_sf = smem + Cfg::ASF_OFF;    // [stage][2 x 512 B]
+    float *recv = reinterpret_cast<float *>(smem + Cfg::RECV_OFF);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::BAR_OFF);
     uint64_t *empty = full + kRing;
-    uint64_t *accf = empty + kRing;
-    uint64_t *act_ready = accf + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(act_ready + 1);
+    uint64_t *act_full = empty + kRing;          // [MAX_ST] quantized operand written
+    uint64_t *accf = act_full + Cfg::MAX_ST;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accf + 1);
     int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -106,8 +120,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(full + s, 1);
             mbar_init(empty + s, 1);
         }
+#pragma unroll
+        for (int s = 0; s < Cfg::MAX_ST; ++s) mbar_init(act_full + s, kQuantThreads);
         mbar_init(accf, 1);
-        mbar_init(act_ready, 128);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmw);
@@ -116,44 +131,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
         tmem_relinquish();
     }
+    // Global memory is touched only after the previous grid in the stream has
+    // completed (programmatic dependent launch overlaps just the prologue).
+    grid_dependency_wait();
+    int issued = 0;
+    const uint64_t pol_w = policy_evict_first();   // weights are read once
+    auto issue_weights = [&](int i) {
+        const int slot = i % kRing;
+        const int ks = s_begin + i;
+        const int blk0 = ks * 2;
+        const int nblk = min(2, p.sf_cblocks - blk0);
+        mbar_arrive_expect_tx(full + slot, kWBytes + nblk * 512);
+        tma_load_2d(ring + slot * kWBytes, &tmw, ks * 128, n_tile * 128, full + slot, pol_w);
+        bulk_load(ring_sf + slot * kWSfBytes, p.sfw + (static_cast<size_t>(n_tile) * p.sf_cblocks + blk0) * 512,
+                  nblk * 512, full + slot, pol_w);
+        issued = i + 1;
+    };
+    if (threadIdx.x == 0) {
+        // the first ring's worth of weight stages go out before the block syncs
+        for (int i = 0; i < min(nst, kRing); ++i) issue_weights(i);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    grid_launch_dependents();
     const uint32_t tmem = *tmem_slot;
-    int issued = 0;
 
     if (warp == 0) {
         if (lane == 0) {
-            // ------------------------------------------ weight TMA producer
-            const uint64_t pol = policy_evict_first();
-            for (int i = 0; i < nst; ++i) {
+            // ------------------------------- weight TMA producer (remaining stages)
+            for (int i = kRing; i < nst; ++i) {
                 const int slot = i % kRing;
-                if (i >= kRing &&
-                    !mbar_wait(empty + slot, ((i / kRing) - 1) & 1, &g_fused_error, kErrWaitEmpty)) {
+                if (!mbar_wait(empty + slot, ((i / kRing) - 1) & 1, &g_fused_error, kErrWaitEmpty)) {
                     *abort_flag = 1;
                     break;
                 }
-                const int ks = s_begin + i;
-                const int blk0 = ks * 2;
-                const int nblk = min(2, p.sf_cblocks - blk0);
-                mbar_arrive_expect_tx(full + slot, kWBytes + nblk * 512);
-                tma_load_2d(ring + slot * kWBytes, &tmw, ks * 128, n_tile * 128, full + slot, pol);
-                bulk_load(ring_sf + slot * kWSfBytes,
-                          p.sfw + (static_cast<size_t>(n_tile) * p.sf_cblocks + blk0) * 512, nblk * 512,
-                          full + slot, pol);
-                issued = i + 1;
+                issue_weights(i);
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------- MMA issuer
             constexpr uint32_t IDESC = idesc_block_scaled(MMA_N, true);
-            bool ok = mbar_wait(act_ready, 0, &g_fused_error, kErrWaitOperand);
-            if (!ok) *abort_flag = 1;
-            tc_fence_after();
-            for (int i = 0; ok && i < nst; ++i) {
+            for (int i = 0; i < nst; ++i) {
                 const int slot = i % kRing;
-                if (!mbar_wait(full + slot, (i / kRing) & 1, &g_fused_error, kErrWaitFull)) {
+                if (!mbar_wait(act_full + i, 0, &g_fused_error, kErrWaitOperand) ||
+                    !mbar_wait(full + slot, (i / kRing) & 1, &g_fused_error, kErrWaitFull)) {
                     *abort_flag = 1;
                     break;
                 }
@@ -183,41 +206,59 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit(accf);
         }
     } else {
-        // ------------------------------- on-chip quantization of A (warps 2-5)
+        // ----------------------------------- on-chip quantization of A (warps 2-5)
+        // Thread tq owns, in every stage, the 32-element blocks u = tq + 128 * e
+        // (e < UPS) of the stage's MMA_N x 8 blocks: row m = u / 8, block j = u % 8.
+        // Rows >= M and blocks past K are zero: they quantize to code 0 with
+        // scale byte 0, which the MMA needs as padding.
         const int tq = threadIdx.x - 64;
-        const int sub = tq & 3;
-        const int per_row = nst * 8;                 // 32-blocks per row in this K-slice
-        const int units = MMA_N * per_row;
-        for (int u0 = 0; u0 < units; u0 += 32) {
-            const int u = u0 + (tq >> 2);
-            const bool active = u < units;
-            const int m = active ? u / per_row : 0;
-            const int lb = active ? u - m * per_row : 0;
-            const int kblk = s_begin * 8 + lb;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (active && m < p.M && kblk * 32 < p.K)
-                v = ld_nc_v4(p.A + static_cast<int64_t>(m) * p.lda + static_cast<int64_t>(kblk) * 32 + sub * 8);
-            uint32_t amax = max_abs_bits8(v);
-            amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-            amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-            const uint32_t sbyte = e8m0_byte_from_amax(amax);
-            const uint32_t codes = mx_codes8(v, sbyte);
-            if (active) {
-                const int t = lb >> 3, j = lb & 7;
-                *reinterpret_cast<uint32_t *>(act + t * Cfg::ACT_TILE + m * 128 + ((j ^ (m & 7)) << 4) + sub * 4) =
-                    codes;
-                if (sub == 0)
-                    act_sf[t * 1024 + (j >> 2) * 512 + (m & 31) * 16 + (m >> 5) * 4 + (j & 3)] =
-                        static_cast<uint8_t>(sbyte);
+        constexpr int UPS = Cfg::UPS;
+        const int total = nst * UPS;                  // this thread's blocks, stage-major
+        for (int b0 = 0; b0 < total; b0 += kBatch) {
+            uint4 v[kBatch][4];
+#pragma unroll
+            for (int x = 0; x < kBatch; ++x) {
+                const int idx = b0 + x;
+                const int t = idx / UPS;
+                const int u = tq + kQuantThreads * (idx - t * UPS);
+                const int m = u >> 3, j = u & 7;
+                const int k0 = (s_begin + t) * 256 + j * 32;
+                const bool ok = idx < total && m < p.M && k0 < p.K;
+                const uint16_t *src = p.A + static_cast<int64_t>(m) * p.lda + k0;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) v[x][q] = ok ? ld_nc_v4(src + q * 8) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int x = 0; x < kBatch; ++x) {
+                const int idx = b0 + x;
+                if (idx >= total) break;
+                const int t = idx / UPS;
+                const int u = tq + kQuantThreads * (idx - t * UPS);
+                const int m = u >> 3, j = u & 7;
+                const uint32_t pair = umax16x2(umax16x2(max_abs_pair8(v[x][0]), max_abs_pair8(v[x][1])),
+                                               umax16x2(max_abs_pair8(v[x][2]), max_abs_pair8(v[x][3])));
+                const uint32_t amax = max(pair & 0xFFFFu, pair >> 16);
+                const uint32_t sbyte = e8m0_byte_from_amax(amax);
+                uint4 codes;
+                codes.x = mx_codes8(v[x][0], sbyte);
+                codes.y = mx_codes8(v[x][1], sbyte);
+                codes.z = mx_codes8(v[x][2], sbyte);
+                codes.w = mx_codes8(v[x][3], sbyte);
+                *reinterpret_cast<uint4 *>(act + t * Cfg::ACT_TILE + m * 128 + ((j ^ (m & 7)) << 4)) = codes;
+                act_sf[t * 1024 + (j >> 2) * 512 + (m & 31) * 16 + (m >> 5) * 4 + (j & 3)] =
+                    static_cast<uint8_t>(sbyte);
+                if ((idx + 1) % UPS == 0) {       // this thread's part of stage t is written
+                    fence_proxy_async_smem();
+                    mbar_arrive(act_full + t);
+                }
             }
         }
-        fence_proxy_async_smem();
-        mbar_arrive(act_ready);
     }
     __syncwarp();
 
     // -------------------------------------------------------------- epilogue
-    float *red = reinterpret_cast<float *>(ring);   // [MMA_N][128] fp32 after the mainloop
+    const int S = p.splits;
+    const int nper = (128 + S - 1) / S;           // weight rows each CTA of the cluster owns
     if (warp >= 2) {
         const bool acc_ok = mbar_wait(accf, 0, &g_fused_error, kErrWaitAccum);
         tc_fence_after();
@@ -225,13 +266,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n_local = q * 32 + lane;
         const int n = n_tile * 128 + n_local;
         const uint32_t t_row = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        const int owner = n_local / nper;
+        const uint32_t dst_base =
+            S > 1 ? mapa_shared(smem_u32(recv) + static_cast<uint32_t>(split * MMA_N * nper + (n_local - owner * nper)) * 4,
+                                static_cast<uint32_t>(owner))
+                  : 0u;
 #pragma unroll 1
         for (int c0 = 0; c0 < MMA_N; c0 += 16) {
             uint32_t v[16];
             tmem_ld16(t_row + c0, v);
             tmem_ld_wait();
             if (!acc_ok) continue;
-            if (p.splits == 1) {
+            if (S == 1) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int m = c0 + j;
@@ -240,41 +286,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) red[(c0 + j) * 128 + n_local] = __uint_as_float(v[j]);
+                for (int j = 0; j < 16; ++j)
+                    if (c0 + j < p.M) st_shared_cluster_f32(dst_base + (c0 + j) * nper * 4, __uint_as_float(v[j]));
             }
         }
         if (!acc_ok) *abort_flag = 1;
     }
 
-    if (p.splits > 1) {
-        // every CTA of the cluster reaches both barriers, also after an abort
+    if (S > 1) {
+        // every CTA of the cluster reaches the barrier, also after an abort
         cluster_sync();
-        const int rank = static_cast<int>(cluster_ctarank());
-        const int nper = (128 + p.splits - 1) / p.splits;
-        const int n_lo = rank * nper;
-        const int n_hi = min(128, n_lo + nper);
-        const int width = n_hi - n_lo;
-        const uint32_t red_base = smem_u32(red);
+        const int n_lo = split * nper;
+        const int width = min(128, n_lo + nper) - n_lo;
         if (width > 0) {
             const int cnt = width * p.M;
             for (int idx = threadIdx.x; idx < cnt; idx += kThreads) {
                 const int m = idx / width;
-                const int nl = n_lo + (idx - m * width);
-                const int n = n_tile * 128 + nl;
+                const int nl = idx - m * width;
+                const int n = n_tile * 128 + n_lo + nl;
                 if (n >= p.N) continue;
-                const uint32_t addr = red_base + static_cast<uint32_t>((m * 128 + nl) * 4);
                 float s = 0.0f;
-                for (int r = 0; r < p.splits; ++r) s += ld_shared_cluster_f32(mapa_shared(addr, r));
+                for (int r = 0; r < S; ++r) s += recv[(r * MMA_N + m) * nper + nl];
                 p.C[static_cast<int64_t>(m) * p.ldc + n] = __float2bfloat16_rn(s);
             }
         }
-        cluster_sync();
     }
 
     // -------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
     if (warp == 0 && lane == 0) {
+        // copies still in flight (only after an abort) must land before exit
         for (int i = max(0, issued - kRing); i < issued; ++i)
             mbar_wait(full + (i % kRing), (i / kRing) & 1, &g_fused_error, kErrWaitDrain);
     }
@@ -297,8 +339,6 @@ cudaError_t launch_fused_t(const CUtensorMap &tmw, const FusedArgs &args, int n_
     if (!(configured & (1ull << (dev & 63)))) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
         configured |= 1ull << (dev & 63);
     }
     cudaLaunchConfig_t cfg;
@@ -307,13 +347,15 @@ cudaError_t launch_fused_t(const CUtensorMap &tmw, const FusedArgs &args, int n_
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = splits;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, tmw, args);
 }
 
@@ -323,11 +365,11 @@ bool plan_fused(int64_t M, int64_t N, int64_t K, int num_sms, FusedPlan *plan)
 {
     if (M < 1 || M > 64 || N < 1 || K < 32) return false;
     const int mma_n = M <= 16 ? 16 : M <= 32 ? 32 : 64;
-    const int max_st = FusedCfg<16>::MAX_ST;
+    const int max_st = mma_n == 16 ? FusedCfg<16>::MAX_ST : mma_n == 32 ? FusedCfg<32>::MAX_ST : FusedCfg<64>::MAX_ST;
     const int64_t k_stages = (K + 255) / 256;
     const int64_t n_tiles = (N + 127) / 128;
     int64_t s = (num_sms + n_tiles / 2) / n_tiles;
-    if (s > 8) s = 8;
+    if (s > kMaxSplits) s = kMaxSplits;
     if (s < 1) s = 1;
     if (s > k_stages) s = k_stages;
     const int64_t s_min = (k_stages + max_st - 1) / max_st;
@@ -339,9 +381,8 @@ bool plan_fused(int64_t M, int64_t N, int64_t K, int num_sms, FusedPlan *plan)
     return true;
 }
 
-cudaError_t launch_fused_mx(const CUtensorMap &tmb, const void *A, int64_t lda, const uint8_t *sfb,
-                            void *C, int64_t ldc, int M, int N, int K, const FusedPlan &plan,
-                            cudaStream_t stream)
+cudaError_t launch_fused_mx(const CUtensorMap &tmb, const void *A, int64_t lda, const uint8_t *sfb, void *C,
+                            int64_t ldc, int M, int N, int K, const FusedPlan &plan, cudaStream_t stream)
 {
     FusedArgs a;
     a.A = static_cast<const uint16_t *>(A);

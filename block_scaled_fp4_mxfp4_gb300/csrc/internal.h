@@ -48,9 +48,10 @@ struct FusedPlan {
 };
 // Whether the fused small-M kernel can run (M, K) and with which plan.
 bool plan_fused(int64_t M, int64_t N, int64_t K, int num_sms, FusedPlan *plan);
-cudaError_t launch_fused_mx(const CUtensorMap &tmb, const void *A, int64_t lda,
-                            const uint8_t *sfb, void *C, int64_t ldc, int M, int N, int K,
-                            const FusedPlan &plan, cudaStream_t stream);
+// tmb: packed weights [N, K/2], box {128 B, 128 rows}, 128B swizzle.
+cudaError_t launch_fused_mx(const CUtensorMap &tmb, const void *A, int64_t lda, const uint8_t *sfb,
+                            void *C, int64_t ldc, int M, int N, int K, const FusedPlan &plan,
+                            cudaStream_t stream);
 int read_and_clear_fused_error();
 
 }  // namespace mxfp4

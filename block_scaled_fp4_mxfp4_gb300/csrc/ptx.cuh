@@ -280,6 +280,16 @@ __device__ __forceinline__ uint32_t idesc_with_sf_ids(uint32_t idesc, uint32_t a
     return idesc | (a_id << 29) | (b_id << 4);
 }
 
+// ------------------------------------------- programmatic dependent launch
+
+// Blocks until the grids this launch depends on have completed and their
+// memory is visible (returns at once when launched without that dependency).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next grid in the stream be scheduled before this one finishes; it
+// still waits in grid_dependency_wait() for this grid's results.
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------- cluster helpers
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
@@ -301,17 +311,16 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank)
     return r;
 }
 
-__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr)
+// Store to the shared memory of a CTA in this cluster (address from mapa).
+__device__ __forceinline__ void st_shared_cluster_f32(uint32_t addr, float v)
 {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
 // ------------------------------------------------------------ FP4 encoding
 
-// E2M1 code pair of two non-negative fp32 values (round-to-nearest-even,
-// saturating at 6): `lo` goes to bits 0-3, `hi` to bits 4-7.
+// E2M1 code pair of two fp32 values (round-to-nearest-even, saturating at
+// +-6): `lo` goes to bits 0-3, `hi` to bits 4-7.
 __device__ __forceinline__ uint32_t e2m1x2_rn_sat(float lo, float hi)
 {
     uint16_t r;

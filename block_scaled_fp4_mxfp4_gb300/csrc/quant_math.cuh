@@ -15,17 +15,26 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void *p)
     return v;
 }
 
+// Lane-wise unsigned 16-bit max of two packed pairs.
+__device__ __forceinline__ uint32_t umax16x2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Packed (two-lane) maximum bf16 magnitude of 8 values; bf16 magnitudes
+// compare like unsigned integers once the sign bit is cleared.
+__device__ __forceinline__ uint32_t max_abs_pair8(const uint4 &v)
+{
+    return umax16x2(umax16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                    umax16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+}
+
 __device__ __forceinline__ uint32_t max_abs_bits8(const uint4 &v)
 {
-    // bf16 magnitudes compare like unsigned integers
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t m = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        m = max(m, w[i] & 0x7FFFu);
-        m = max(m, (w[i] >> 16) & 0x7FFFu);
-    }
-    return m;
+    const uint32_t m = max_abs_pair8(v);
+    return max(m & 0xFFFFu, m >> 16);
 }
 
 // E8M0 byte of a block whose largest magnitude has bf16 bits `amax_bits`:
@@ -37,39 +46,38 @@ __device__ __forceinline__ uint32_t e8m0_byte_from_amax(uint32_t amax_bits)
     return E >= 2 ? E - 2 : 0;
 }
 
-// Codes of 8 bf16 values scaled by 2^(127 - sbyte) (exact power-of-two scale).
+// Codes of 8 bf16 values scaled by 2^(127 - sbyte) (exact power-of-two
+// scale). The conversion takes the signed values, so a negative value that
+// rounds to zero keeps its sign (code 0x8), as -0 does.
 __device__ __forceinline__ uint32_t mx_codes8(const uint4 &v, uint32_t sbyte)
 {
     const float mult = __uint_as_float((254u - sbyte) << 23);  // 2^-e, e = sbyte - 127
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t out = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const uint32_t lo = w[i] & 0xFFFFu, hi = w[i] >> 16;
-        const float flo = __uint_as_float((lo & 0x7FFFu) << 16) * mult;
-        const float fhi = __uint_as_float((hi & 0x7FFFu) << 16) * mult;
-        uint32_t byte = e2m1x2_rn_sat(flo, fhi);
-        byte |= ((lo >> 15) << 3) | ((hi >> 15) << 7);
-        out |= byte << (8 * i);
+        const float flo = __uint_as_float(w[i] << 16) * mult;
+        const float fhi = __uint_as_float(w[i] & 0xFFFF0000u) * mult;
+        out |= e2m1x2_rn_sat(flo, fhi) << (8 * i);
     }
     return out;
 }
 
+// Codes of 8 bf16 values divided by the decoded E4M3 scale s (fp32 division,
+// round-to-nearest-even); s == 0 leaves signed zeros.
 __device__ __forceinline__ uint32_t nv_codes8(const uint4 &v, float s)
 {
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t out = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const uint32_t lo = w[i] & 0xFFFFu, hi = w[i] >> 16;
-        float flo = 0.0f, fhi = 0.0f;
+        float flo = __uint_as_float((w[i] << 16) & 0x80000000u);
+        float fhi = __uint_as_float(w[i] & 0x80000000u);
         if (s > 0.0f) {
-            flo = __fdiv_rn(__uint_as_float((lo & 0x7FFFu) << 16), s);
-            fhi = __fdiv_rn(__uint_as_float((hi & 0x7FFFu) << 16), s);
+            flo = __fdiv_rn(__uint_as_float(w[i] << 16), s);
+            fhi = __fdiv_rn(__uint_as_float(w[i] & 0xFFFF0000u), s);
         }
-        uint32_t byte = e2m1x2_rn_sat(flo, fhi);
-        byte |= ((lo >> 15) << 3) | ((hi >> 15) << 7);
-        out |= byte << (8 * i);
+        out |= e2m1x2_rn_sat(flo, fhi) << (8 * i);
     }
     return out;
 }
