@@ -417,3 +417,76 @@ mxfp4_status_t mxfp4_get_device_error(int *code)
 }
 
 }  // extern "C"
+
+// ----------------------------------------------------------------------------
+// mxfp4_gemm_a4w4_noalloc: the MXFP4 GEMM with its split-K scratch (fp32
+// partial sums and per-tile tickets) in a fixed device array owned by this
+// library, for callers that cannot allocate device memory themselves.
+
+namespace {
+
+// Scratch of the no-allocation GEMM. Every GPU that loads the library holds
+// these bytes until the process exits; all calls share them.
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[64] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device (host code only sees a stand-in symbol, never the address).
+mxfp4_status_t noalloc_scratch(void **out)
+{
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64) return MXFP4_ERR_NO_DEVICE;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[d]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MXFP4_ERR_CUDA;
+        g_noalloc_ptr[d] = p;
+    }
+    *out = g_noalloc_ptr[d];
+    return MXFP4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mxfp4_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
+
+mxfp4_status_t mxfp4_gemm_a4w4_noalloc(const void *Aq, int64_t ldaq, const void *A_sf, const void *Bq,
+                                       int64_t ldbq, const void *B_sf, void *C, int64_t ldc, int64_t M,
+                                       int64_t N, int64_t K, void *stream)
+{
+    mxfp4_status_t st = check_gemm_common(Bq, ldbq, B_sf, C, ldc, M, N, K);
+    if (st != MXFP4_OK) return st;
+    if (!Aq || !A_sf) return MXFP4_ERR_INVALID_ARG;
+    if (ldaq < K / 2) return MXFP4_ERR_INVALID_ARG;
+    if (ldaq % 16 != 0 || !al16(Aq) || !al16(A_sf)) return MXFP4_ERR_MISALIGNED;
+    // scratch this shape needs: split-K partials, then one ticket per tile
+    const GemmPlan gp = plan_gemm(M, N, K);
+    WsLayout wl;
+    memset(&wl, 0, sizeof(wl));
+    size_t part = 0;
+    if (gp.splits > 1)
+        part = static_cast<size_t>(gp.splits) * gp.n_tiles * gemm_block_n(false) * static_cast<size_t>(M) * 4;
+    wl.part_off = 0;
+    wl.ticket_off = up256(part);
+    wl.total = wl.ticket_off + up256(static_cast<size_t>(gp.tiles) * 4);
+    if (wl.total > kNoAllocScratchBytes) return MXFP4_ERR_WORKSPACE_TOO_SMALL;
+    int sms = 0;
+    st = current_device(&sms);
+    if (st != MXFP4_OK) return st;
+    void *scratch = nullptr;
+    st = noalloc_scratch(&scratch);
+    if (st != MXFP4_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the tile tickets must start at zero; the array keeps whatever the last call left
+    if (cudaMemsetAsync(static_cast<uint8_t *>(scratch) + wl.ticket_off, 0, static_cast<size_t>(gp.tiles) * 4, s) !=
+        cudaSuccess)
+        return MXFP4_ERR_CUDA;
+    return run_gemm(Aq, ldaq, A_sf, Bq, ldbq, B_sf, C, ldc, M, N, K, scratch, wl, s);
+}
+
+}  // extern "C"

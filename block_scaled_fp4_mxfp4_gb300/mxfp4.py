@@ -68,6 +68,10 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.mxfp4_quant_gemm_fused.argtypes = [_p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p, _sz, _p]
     L.nvfp4_group_gemm.restype = _st
     L.nvfp4_group_gemm.argtypes = [ctypes.POINTER(NvProblem), ctypes.c_int, _p, _sz, _p]
+    L.mxfp4_noalloc_scratch_bytes.restype = _sz
+    L.mxfp4_noalloc_scratch_bytes.argtypes = []
+    L.mxfp4_gemm_a4w4_noalloc.restype = _st
+    L.mxfp4_gemm_a4w4_noalloc.argtypes = [_p, _i64, _p, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p]
     L.mxfp4_get_device_error.restype = _st
     L.mxfp4_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
     return L
@@ -169,6 +173,20 @@ def mxfp4_gemm_a4w4(Aq, A_sf, Bq, B_sf, K: int, C=None, workspace=None, stream=N
                                 Bq.stride(0), B_sf.data_ptr(), C.data_ptr(), C.stride(0), M, N, K,
                                 workspace.data_ptr(), workspace.numel(), _stream_ptr(stream)),
            "mxfp4_gemm_a4w4")
+    return C
+
+
+def mxfp4_gemm_a4w4_noalloc(Aq, A_sf, Bq, B_sf, K: int, C, stream=None):
+    """The MXFP4 GEMM with the library's fixed scratch array instead of a workspace,
+    for callers that cannot allocate device memory (C must be given)."""
+    _dev(Aq, "Aq", torch.uint8, 2)
+    _dev(Bq, "Bq", torch.uint8, 2)
+    _dev(C, "C", torch.bfloat16, 2)
+    M, N = Aq.shape[0], Bq.shape[0]
+    _check(_lib.mxfp4_gemm_a4w4_noalloc(Aq.data_ptr(), Aq.stride(0), A_sf.data_ptr(), Bq.data_ptr(),
+                                        Bq.stride(0), B_sf.data_ptr(), C.data_ptr(), C.stride(0), M, N, K,
+                                        _stream_ptr(stream)),
+           "mxfp4_gemm_a4w4_noalloc")
     return C
 
 

@@ -180,6 +180,35 @@ MXFP4_API size_t nvfp4_group_workspace_bytes(int num_groups);
 MXFP4_API mxfp4_status_t nvfp4_group_gemm(const nvfp4_problem_t *problems, int num_groups, void *workspace,
                                 size_t ws_bytes, void *stream);
 
+/* Bytes of the fixed device scratch array behind mxfp4_gemm_a4w4_noalloc
+ * (8 MiB). */
+MXFP4_API size_t mxfp4_noalloc_scratch_bytes(void);
+
+/* The MXFP4 GEMM of mxfp4_gemm_a4w4 for callers that cannot allocate device
+ * memory -- for example a plugin running inside an engine that owns every
+ * device allocation and hands it no scratch buffer, or a program whose memory
+ * plan is fixed at start-up. There is no counterpart on the source pages; it
+ * is a convenience of this library.
+ *   Same arguments and result as mxfp4_gemm_a4w4, without the workspace: the
+ *   split-K scratch (fp32 partial sums and per-tile counters) lives in one
+ *   static device array of mxfp4_noalloc_scratch_bytes() bytes inside the
+ *   library, which every GPU that loads the library keeps until the process
+ *   exits. The call allocates nothing; it clears the counters with an
+ *   asynchronous memset on `stream` before the GEMM.
+ *   Shapes whose scratch would exceed the array return
+ *   MXFP4_ERR_WORKSPACE_TOO_SMALL before anything is enqueued (use
+ *   mxfp4_gemm_a4w4 with a caller workspace for those).
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) once for that device; make that first call before
+ *   any stream capture. All calls share the array and it keeps the last
+ *   call's contents: calls that overlap on the GPU (other streams, other host
+ *   threads without ordering) race on it and must be serialized by the
+ *   caller. */
+MXFP4_API mxfp4_status_t mxfp4_gemm_a4w4_noalloc(const void *Aq, int64_t ldaq, const void *A_sf,
+                                                 const void *Bq, int64_t ldbq, const void *B_sf,
+                                                 void *C, int64_t ldc, int64_t M, int64_t N,
+                                                 int64_t K, void *stream);
+
 /* ------------------------------------------------------------ diagnostics -- */
 
 /* Reads and clears the library's device-side error word. Kernels never trap:
