@@ -11,14 +11,17 @@
 // * Grid = (ceil(N/128) weight tiles) x (S K-splits); the S CTAs of one weight
 //   tile form a thread-block cluster. Each CTA streams its K-slice of 128
 //   weight rows through a 4-slot TMA ring (evict-first: weights are read once).
-// * Warps 2-5 read the CTA's K-slice of bf16 A straight from global memory,
-//   all of a batch's loads in flight at once. A thread owns whole 32-element
-//   blocks (row m, block j): it forms the OCP MX scale and the 32 E2M1 codes
-//   with the same arithmetic as the standalone quant kernel and writes them
-//   into shared memory directly in the MMA's 128-byte-swizzled K-major operand
-//   layout (16 bytes per block), plus the scale in the 512-byte blocked layout.
-//   Each K-stage is released to the MMA issuer as soon as it is written.
-// * Warp 1 lane 0 copies both operands' scales to TMEM and issues the MMAs.
+// * Warps 2-5 are stage warps: warp 2 + w owns the CTA's K-stages w, w + 4, ...
+//   Its lanes read the stage's bf16 A straight from global memory (a batch of
+//   loads in flight per lane), form the OCP MX scale and the E2M1 codes of each
+//   32-element block with the same arithmetic as the standalone quant kernel,
+//   and write them into shared memory directly in the MMA's 128-byte-swizzled
+//   K-major operand layout, plus the scales in the 512-byte blocked layout.
+//   Lane 0 then copies both operands' scales to TMEM and issues the stage's
+//   MMAs into the warp's own TMEM accumulator. Issuing a tcgen05 instruction
+//   costs on the order of 100 cycles while an N = 16 MMA is only a few cycles
+//   of tensor work, so the four stage warps issue in parallel and the
+//   epilogue sums their accumulators.
 // * Split-K reduction without global scratch: every CTA pushes the slice of
 //   its fp32 tile that CTA r of the cluster owns (weight rows r*128/S ..) into
 //   r's shared memory with remote stores; after one cluster barrier each CTA
@@ -42,9 +45,9 @@ constexpr int kRing = 4;
 constexpr uint32_t kWBytes = 128 * 128;   // one stage of 128 weight rows x 256 FP4
 constexpr uint32_t kWSfBytes = 2 * 512;   // its two 512-byte scale blocks
 constexpr int kThreads = 192;
-constexpr int kQuantThreads = 128;        // warps 2-5
+constexpr int kStageWarps = 4;           // warps 2-5: quantize + issue MMAs
 constexpr int kMaxSplits = 8;             // portable cluster size
-constexpr int kBatch = 4;                 // 32-element blocks a quant thread keeps in flight
+constexpr int kBatch = 4;                 // 32-element blocks a lane keeps in flight
 
 __host__ __device__ constexpr uint32_t pow2_cols_f(uint32_t n)
 {
@@ -53,10 +56,11 @@ __host__ __device__ constexpr uint32_t pow2_cols_f(uint32_t n)
 
 template <int MMA_N>
 struct FusedCfg {
-    // K stages (256 wide) held per CTA: each has its own quantized operand tile.
+    // K stages (256 wide) held per CTA: each has its own quantized operand tile
+    // and its own TMEM scale columns.
     static constexpr int MAX_ST = MMA_N <= 16 ? 8 : 4;
-    static constexpr int UPS = MMA_N * 8 / kQuantThreads;  // blocks per quant thread per stage
-    static constexpr uint32_t ACT_TILE = MMA_N * 128;      // quantized operand bytes per stage
+    static constexpr int BPL = MMA_N * 8 / 32;              // 32-blocks per lane per stage
+    static constexpr uint32_t ACT_TILE = MMA_N * 128;       // quantized operand bytes per stage
     static constexpr uint32_t RING_DATA = kRing * kWBytes;
     static constexpr uint32_t ACT_OFF = RING_DATA;
     static constexpr uint32_t WSF_OFF = ACT_OFF + MAX_ST * ACT_TILE;
@@ -66,12 +70,14 @@ struct FusedCfg {
     static constexpr uint32_t RECV_BYTES = MMA_N * (128 + kMaxSplits) * 4;
     static constexpr uint32_t BAR_OFF = RECV_OFF + RECV_BYTES;
     static constexpr uint32_t SMEM_BYTES = BAR_OFF + 256 + 1024;
-    static constexpr uint32_t SF_COLS = 16;                 // 8 weight + 8 activation per slot
-    static constexpr uint32_t TMEM_COLS = pow2_cols_f(MMA_N + kRing * SF_COLS);
-    static_assert(UPS >= 1 && kBatch % UPS == 0, "quant work split");
+    static constexpr uint32_t SF_COLS = 16;                  // per stage: 8 weight + 8 activation
+    static constexpr uint32_t ACC_COLS = kStageWarps * MMA_N;  // one accumulator per stage warp
+    static constexpr uint32_t TMEM_COLS = pow2_cols_f(ACC_COLS + MAX_ST * SF_COLS);
+    static_assert(BPL % kBatch == 0, "quant work split");
     static_assert(ACT_TILE % 1024 == 0, "swizzled operand tiles need 1024-byte alignment");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-    static_assert((2 * kRing + MAX_ST + 1) * 8 + 8 <= 256, "barrier area");
+    static_assert(ACC_COLS + MAX_ST * SF_COLS <= 512, "TMEM budget");
+    static_assert((2 * kRing + 1) * 8 + 8 <= 256, "barrier area");
 };
 
 struct FusedArgs {
@@ -99,8 +105,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     float *recv = reinterpret_cast<float *>(smem + Cfg::RECV_OFF);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::BAR_OFF);
     uint64_t *empty = full + kRing;
-    uint64_t *act_full = empty + kRing;          // [MAX_ST] quantized operand written
-    uint64_t *accf = act_full + Cfg::MAX_ST;
+    uint64_t *accf = empty + kRing;              // one arrival per stage warp
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accf + 1);
     int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
@@ -114,26 +119,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int nst = s_end - s_begin;
     const int k_steps_total = (p.K + 63) / 64;
 
-    if (threadIdx.x == 0) {
-#pragma unroll
-        for (int s = 0; s < kRing; ++s) {
-            mbar_init(full + s, 1);
-            mbar_init(empty + s, 1);
-        }
-#pragma unroll
-        for (int s = 0; s < Cfg::MAX_ST; ++s) mbar_init(act_full + s, kQuantThreads);
-        mbar_init(accf, 1);
-        *abort_flag = 0;
-        fence_mbar_init();
-        tma_prefetch_desc(&tmw);
-    }
-    if (warp == 1) {
-        tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
-        tmem_relinquish();
-    }
-    // Global memory is touched only after the previous grid in the stream has
-    // completed (programmatic dependent launch overlaps just the prologue).
-    grid_dependency_wait();
     int issued = 0;
     const uint64_t pol_w = policy_evict_first();   // weights are read once
     auto issue_weights = [&](int i) {
@@ -148,9 +133,35 @@ __global__ void __launch_bounds__(kThreads, 2)
         issued = i + 1;
     };
     if (threadIdx.x == 0) {
-        // the first ring's worth of weight stages go out before the block syncs
+#pragma unroll
+        for (int s = 0; s < kRing; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        mbar_init(accf, kStageWarps);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmw);
+        // Weights are read-only inputs that no kernel of this library writes,
+        // so the first ring's worth of weight stages is requested before the
+        // grid-dependency wait: under programmatic dependent launch the stream
+        // of weights overlaps the tail of the preceding call.
         for (int i = 0; i < min(nst, kRing); ++i) issue_weights(i);
     }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (threadIdx.x >= 64 && threadIdx.x - 64 < p.M && nst > 0) {
+        // Warm L2 with this CTA's rows of A while the preceding grid finishes;
+        // the loads that use A still wait for that grid below.
+        const int64_t k0 = static_cast<int64_t>(s_begin) * 256;
+        const int64_t k1 = min(static_cast<int64_t>(s_end) * 256, static_cast<int64_t>(p.K));
+        prefetch_l2_bulk(p.A + static_cast<int64_t>(threadIdx.x - 64) * p.lda + k0, static_cast<uint32_t>((k1 - k0) * 2));
+    }
+    // A, C and everything else in global memory is touched only after the
+    // preceding grid in the stream has completed and its writes are visible.
+    grid_dependency_wait();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -159,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (warp == 0) {
         if (lane == 0) {
-            // ------------------------------- weight TMA producer (remaining stages)
+            // ------------------------------- weight TMA producer (stages past the ring)
             for (int i = kRing; i < nst; ++i) {
                 const int slot = i % kRing;
                 if (!mbar_wait(empty + slot, ((i / kRing) - 1) & 1, &g_fused_error, kErrWaitEmpty)) {
@@ -169,89 +180,91 @@ __global__ void __launch_bounds__(kThreads, 2)
                 issue_weights(i);
             }
         }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------- MMA issuer
-            constexpr uint32_t IDESC = idesc_block_scaled(MMA_N, true);
-            for (int i = 0; i < nst; ++i) {
-                const int slot = i % kRing;
-                if (!mbar_wait(act_full + i, 0, &g_fused_error, kErrWaitOperand) ||
-                    !mbar_wait(full + slot, (i / kRing) & 1, &g_fused_error, kErrWaitFull)) {
+    } else if (warp >= 2) {
+        // --------------- stage warps: quantize a K-stage of A, then issue its MMAs
+        // Stage warp sw owns stages t = sw, sw + 4, ...: its lanes quantize the
+        // stage's MMA_N x 8 blocks of 32 elements (lane owns blocks lane + 32 e),
+        // writing codes in the MMA's 128-byte-swizzled K-major layout and scales
+        // in the blocked layout; lane 0 then copies both operands' scales to
+        // TMEM and issues the stage's four MMAs into the warp's own accumulator,
+        // so the stages of a CTA are quantized and issued in parallel. Rows >= M
+        // and blocks past K are zero and quantize to code 0 with scale byte 0.
+        const int sw = warp - 2;
+        const uint32_t acc_tmem = tmem + static_cast<uint32_t>(sw * MMA_N);
+        constexpr uint32_t IDESC = idesc_block_scaled(MMA_N, true);
+        bool first = true;
+        for (int t = sw; t < nst; t += kStageWarps) {
+            const int ks = s_begin + t;
+            uint8_t *dst = act + t * Cfg::ACT_TILE;
+            uint8_t *dsf = act_sf + t * 1024;
+#pragma unroll 1
+            for (int e0 = 0; e0 < Cfg::BPL; e0 += kBatch) {
+                uint4 v[kBatch][4];
+#pragma unroll
+                for (int x = 0; x < kBatch; ++x) {
+                    const int u = lane + 32 * (e0 + x);
+                    const int m = u >> 3, j = u & 7;
+                    const int k0 = ks * 256 + j * 32;
+                    const bool ok = m < p.M && k0 < p.K;
+                    const uint16_t *src = p.A + static_cast<int64_t>(m) * p.lda + k0;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) v[x][q] = ok ? ld_nc_v4(src + q * 8) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int x = 0; x < kBatch; ++x) {
+                    const int u = lane + 32 * (e0 + x);
+                    const int m = u >> 3, j = u & 7;
+                    const uint32_t pair = umax16x2(umax16x2(max_abs_pair8(v[x][0]), max_abs_pair8(v[x][1])),
+                                                   umax16x2(max_abs_pair8(v[x][2]), max_abs_pair8(v[x][3])));
+                    const uint32_t sbyte = e8m0_byte_from_amax(max(pair & 0xFFFFu, pair >> 16));
+                    uint4 codes;
+                    codes.x = mx_codes8(v[x][0], sbyte);
+                    codes.y = mx_codes8(v[x][1], sbyte);
+                    codes.z = mx_codes8(v[x][2], sbyte);
+                    codes.w = mx_codes8(v[x][3], sbyte);
+                    *reinterpret_cast<uint4 *>(dst + m * 128 + ((j ^ (m & 7)) << 4)) = codes;
+                    dsf[(j >> 2) * 512 + (m & 31) * 16 + (m >> 5) * 4 + (j & 3)] = static_cast<uint8_t>(sbyte);
+                }
+            }
+            fence_proxy_async_smem();   // generic-proxy writes -> visible to tcgen05
+            __syncwarp();
+            if (lane == 0) {
+                const int slot = t % kRing;
+                if (!mbar_wait(full + slot, (t / kRing) & 1, &g_fused_error, kErrWaitFull)) {
                     *abort_flag = 1;
-                    break;
+                } else {
+                    tc_fence_after();
+                    const uint32_t w_base = smem_u32(ring + slot * kWBytes);
+                    const uint32_t a_base = smem_u32(dst);
+                    const uint32_t wsf = smem_u32(ring_sf + slot * kWSfBytes);
+                    const uint32_t asf = smem_u32(dsf);
+                    const uint32_t tsfw = tmem + Cfg::ACC_COLS + t * Cfg::SF_COLS;
+                    const uint32_t tsfa = tsfw + 8;
+                    const int ksteps = min(4, k_steps_total - ks * 4);
+                    const int nblk = (ksteps + 1) / 2;
+                    for (int b = 0; b < nblk; ++b) {
+                        tc_cp_scale_block(tsfw + b * 4, sdesc_scale(wsf + b * 512));
+                        tc_cp_scale_block(tsfa + b * 4, sdesc_scale(asf + b * 512));
+                    }
+                    for (int kk = 0; kk < ksteps; ++kk) {
+                        const uint32_t sfid = static_cast<uint32_t>(kk & 1) * 2u;
+                        const int blk = kk >> 1;
+                        mma_mxf4(acc_tmem, sdesc_sw128(w_base + kk * 32), sdesc_sw128(a_base + kk * 32),
+                                 idesc_with_sf_ids(IDESC, sfid, sfid), tsfw + blk * 4, tsfa + blk * 4,
+                                 (first && kk == 0) ? 0u : 1u);
+                    }
+                    tc_commit(empty + slot);
                 }
-                tc_fence_after();
-                const uint32_t w_base = smem_u32(ring + slot * kWBytes);
-                const uint32_t a_base = smem_u32(act + i * Cfg::ACT_TILE);
-                const uint32_t wsf = smem_u32(ring_sf + slot * kWSfBytes);
-                const uint32_t asf = smem_u32(act_sf + i * 1024);
-                const uint32_t tsfw = tmem + MMA_N + slot * Cfg::SF_COLS;
-                const uint32_t tsfa = tsfw + 8;
-                const int ks = s_begin + i;
-                const int ksteps = min(4, k_steps_total - ks * 4);
-                const int nblk = (ksteps + 1) / 2;
-                for (int b = 0; b < nblk; ++b) {
-                    tc_cp_scale_block(tsfw + b * 4, sdesc_scale(wsf + b * 512));
-                    tc_cp_scale_block(tsfa + b * 4, sdesc_scale(asf + b * 512));
-                }
-                for (int kk = 0; kk < ksteps; ++kk) {
-                    const uint32_t sfid = static_cast<uint32_t>(kk & 1) * 2u;
-                    const int blk = kk >> 1;
-                    mma_mxf4(tmem, sdesc_sw128(w_base + kk * 32), sdesc_sw128(a_base + kk * 32),
-                             idesc_with_sf_ids(IDESC, sfid, sfid), tsfw + blk * 4, tsfa + blk * 4,
-                             (i > 0 || kk > 0) ? 1u : 0u);
-                }
-                tc_commit(empty + slot);
             }
-            tc_commit(accf);
+            first = false;
+            __syncwarp();
         }
-    } else {
-        // ----------------------------------- on-chip quantization of A (warps 2-5)
-        // Thread tq owns, in every stage, the 32-element blocks u = tq + 128 * e
-        // (e < UPS) of the stage's MMA_N x 8 blocks: row m = u / 8, block j = u % 8.
-        // Rows >= M and blocks past K are zero: they quantize to code 0 with
-        // scale byte 0, which the MMA needs as padding.
-        const int tq = threadIdx.x - 64;
-        constexpr int UPS = Cfg::UPS;
-        const int total = nst * UPS;                  // this thread's blocks, stage-major
-        for (int b0 = 0; b0 < total; b0 += kBatch) {
-            uint4 v[kBatch][4];
-#pragma unroll
-            for (int x = 0; x < kBatch; ++x) {
-                const int idx = b0 + x;
-                const int t = idx / UPS;
-                const int u = tq + kQuantThreads * (idx - t * UPS);
-                const int m = u >> 3, j = u & 7;
-                const int k0 = (s_begin + t) * 256 + j * 32;
-                const bool ok = idx < total && m < p.M && k0 < p.K;
-                const uint16_t *src = p.A + static_cast<int64_t>(m) * p.lda + k0;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) v[x][q] = ok ? ld_nc_v4(src + q * 8) : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int x = 0; x < kBatch; ++x) {
-                const int idx = b0 + x;
-                if (idx >= total) break;
-                const int t = idx / UPS;
-                const int u = tq + kQuantThreads * (idx - t * UPS);
-                const int m = u >> 3, j = u & 7;
-                const uint32_t pair = umax16x2(umax16x2(max_abs_pair8(v[x][0]), max_abs_pair8(v[x][1])),
-                                               umax16x2(max_abs_pair8(v[x][2]), max_abs_pair8(v[x][3])));
-                const uint32_t amax = max(pair & 0xFFFFu, pair >> 16);
-                const uint32_t sbyte = e8m0_byte_from_amax(amax);
-                uint4 codes;
-                codes.x = mx_codes8(v[x][0], sbyte);
-                codes.y = mx_codes8(v[x][1], sbyte);
-                codes.z = mx_codes8(v[x][2], sbyte);
-                codes.w = mx_codes8(v[x][3], sbyte);
-                *reinterpret_cast<uint4 *>(act + t * Cfg::ACT_TILE + m * 128 + ((j ^ (m & 7)) << 4)) = codes;
-                act_sf[t * 1024 + (j >> 2) * 512 + (m & 31) * 16 + (m >> 5) * 4 + (j & 3)] =
-                    static_cast<uint8_t>(sbyte);
-                if ((idx + 1) % UPS == 0) {       // this thread's part of stage t is written
-                    fence_proxy_async_smem();
-                    mbar_arrive(act_full + t);
-                }
-            }
+        // one arrival per stage warp once its MMAs are done (at once if it had none)
+        if (lane == 0) {
+            if (first)
+                mbar_arrive(accf);
+            else
+                tc_commit(accf);
         }
     }
     __syncwarp();
@@ -259,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // -------------------------------------------------------------- epilogue
     const int S = p.splits;
     const int nper = (128 + S - 1) / S;           // weight rows each CTA of the cluster owns
+    const int nacc = min(nst, kStageWarps);       // accumulators that hold data
     if (warp >= 2) {
         const bool acc_ok = mbar_wait(accf, 0, &g_fused_error, kErrWaitAccum);
         tc_fence_after();
@@ -273,21 +287,27 @@ __global__ void __launch_bounds__(kThreads, 2)
                   : 0u;
 #pragma unroll 1
         for (int c0 = 0; c0 < MMA_N; c0 += 16) {
-            uint32_t v[16];
-            tmem_ld16(t_row + c0, v);
-            tmem_ld_wait();
+            float f[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) f[j] = 0.0f;
+            for (int a = 0; a < nacc; ++a) {
+                uint32_t v[16];
+                tmem_ld16(t_row + static_cast<uint32_t>(a * MMA_N + c0), v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) f[j] += __uint_as_float(v[j]);
+            }
             if (!acc_ok) continue;
             if (S == 1) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int m = c0 + j;
-                    if (m < p.M && n < p.N)
-                        p.C[static_cast<int64_t>(m) * p.ldc + n] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                    if (m < p.M && n < p.N) p.C[static_cast<int64_t>(m) * p.ldc + n] = __float2bfloat16_rn(f[j]);
                 }
             } else {
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
-                    if (c0 + j < p.M) st_shared_cluster_f32(dst_base + (c0 + j) * nper * 4, __uint_as_float(v[j]));
+                    if (c0 + j < p.M) st_shared_cluster_f32(dst_base + (c0 + j) * nper * 4, f[j]);
             }
         }
         if (!acc_ok) *abort_flag = 1;

@@ -118,6 +118,14 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint
         : "memory");
 }
 
+// Asks L2 to fetch [gsrc, gsrc + bytes) (16-byte aligned, bytes % 16 == 0)
+// without copying it anywhere. L2 is the point of coherence, so a prefetch
+// never makes a later load see stale data.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *gsrc, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first()
 {
     uint64_t p;

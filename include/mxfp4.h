@@ -43,6 +43,13 @@
  *   MXFP4_ERR_CUDA. There is no fallback path of any kind.
  * - Thread safety: calls may come from several host threads; the internal
  *   plan cache is locked.
+ * - Overlap of consecutive calls: GEMM launches use programmatic dependent
+ *   launch. A call may start while the preceding kernel in the stream is
+ *   finishing and may already read its pre-quantized weights (Bq, B_sf) then;
+ *   A, C, the workspace and every write wait until the preceding kernel has
+ *   completed. Only this library's GEMM kernels let a successor start early,
+ *   and they never write weight buffers, so stream order is preserved as
+ *   long as weights are not produced by a GEMM call of this library.
  */
 #ifndef MXFP4_GB300_H
 #define MXFP4_GB300_H
