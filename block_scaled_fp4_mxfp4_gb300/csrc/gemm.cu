@@ -142,7 +142,8 @@ __global__ void __launch_bounds__(128, 1) bs_gemm_kernel(const __grid_constant__
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * Cfg::STAGE_BYTES);
     uint64_t *empty = full + STAGES;
-    uint64_t *accf = empty + STAGES;
+    uint64_t *sf_full = empty + STAGES;   // [STAGES] the stage's scales are in TMEM
+    uint64_t *accf = sf_full + STAGES;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accf + 1);
     int *last_flag = reinterpret_cast<int *>(tmem_slot + 1);
     int *abort_flag = last_flag + 1;
@@ -171,6 +172,7 @@ __global__ void __launch_bounds__(128, 1) bs_gemm_kernel(const __grid_constant__
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full + s, 1);
             mbar_init(empty + s, 1);
+            mbar_init(sf_full + s, 1);
         }
         mbar_init(accf, 1);
         *abort_flag = 0;
@@ -222,10 +224,13 @@ __global__ void __launch_bounds__(128, 1) bs_gemm_kernel(const __grid_constant__
         }
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------------- MMA issuer
+        // Only MMAs are issued here (each tcgen05 instruction costs tens of
+        // cycles to issue); warp 2 stages the scale factors into TMEM.
         constexpr uint32_t IDESC = idesc_block_scaled(BN, MX);
         for (int i = 0; i < nst; ++i) {
             const int slot = i % STAGES;
-            if (!mbar_wait(full + slot, (i / STAGES) & 1, &g_gemm_error, kErrWaitFull)) {
+            if (!mbar_wait(full + slot, (i / STAGES) & 1, &g_gemm_error, kErrWaitFull) ||
+                !mbar_wait(sf_full + slot, (i / STAGES) & 1, &g_gemm_error, kErrWaitFull)) {
                 *abort_flag = 1;
                 break;
             }
@@ -233,20 +238,10 @@ __global__ void __launch_bounds__(128, 1) bs_gemm_kernel(const __grid_constant__
             uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
             const uint32_t a_base = smem_u32(st);
             const uint32_t b_base = smem_u32(st + Cfg::A_BYTES);
-            const uint32_t sfa_s = smem_u32(st + Cfg::A_BYTES + Cfg::B_BYTES);
-            const uint32_t sfb_s = sfa_s + Cfg::SFA_BYTES;
             const uint32_t tsfa = tmem_sf + slot * Cfg::SF_COLS;
             const uint32_t tsfb = tsfa + Cfg::SF_COLS_A;
             const int ks = s_begin + i;
             const int ksteps = min(4, k_steps_total - ks * 4);
-            const int nblk = MX ? (ksteps + 1) / 2 : ksteps;
-            for (int b = 0; b < nblk; ++b) {
-                tc_cp_scale_block(tsfa + b * 4, sdesc_scale(sfa_s + b * 512));
-#pragma unroll
-                for (int j = 0; j < Cfg::NCH; ++j)
-                    tc_cp_scale_block(tsfb + (b * Cfg::NCH + j) * 4,
-                                      sdesc_scale(sfb_s + (j * Cfg::SF_BLK + b) * 512));
-            }
             for (int kk = 0; kk < ksteps; ++kk) {
                 const uint64_t ad = sdesc_sw128(a_base + kk * 32);
                 const uint64_t bd = sdesc_sw128(b_base + kk * 32);
@@ -263,6 +258,35 @@ __global__ void __launch_bounds__(128, 1) bs_gemm_kernel(const __grid_constant__
         }
         // arrives once every MMA issued above has completed (also on abort)
         tc_commit(accf);
+    } else if (warp == 2 && lane == 0) {
+        // ------------------------------------- scale staging, smem -> TMEM
+        // A stage's TMEM scale slot is rewritten only after the stage that
+        // used it has been consumed: its smem slot was refilled, which needed
+        // the MMAs' "empty" commit, so the full wait below orders the copies.
+        for (int i = 0; i < nst; ++i) {
+            const int slot = i % STAGES;
+            if (!mbar_wait(full + slot, (i / STAGES) & 1, &g_gemm_error, kErrWaitFull)) {
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
+            const uint32_t sfa_s = smem_u32(st + Cfg::A_BYTES + Cfg::B_BYTES);
+            const uint32_t sfb_s = sfa_s + Cfg::SFA_BYTES;
+            const uint32_t tsfa = tmem_sf + slot * Cfg::SF_COLS;
+            const uint32_t tsfb = tsfa + Cfg::SF_COLS_A;
+            const int ks = s_begin + i;
+            const int ksteps = min(4, k_steps_total - ks * 4);
+            const int nblk = MX ? (ksteps + 1) / 2 : ksteps;
+            for (int b = 0; b < nblk; ++b) {
+                tc_cp_scale_block(tsfa + b * 4, sdesc_scale(sfa_s + b * 512));
+#pragma unroll
+                for (int j = 0; j < Cfg::NCH; ++j)
+                    tc_cp_scale_block(tsfb + (b * Cfg::NCH + j) * 4,
+                                      sdesc_scale(sfb_s + (j * Cfg::SF_BLK + b) * 512));
+            }
+            tc_commit(sf_full + slot);
+        }
     }
     __syncwarp();
 
