@@ -85,56 +85,70 @@ struct GemmCfg {
 };
 
 template <bool F16>
-__device__ __forceinline__ void store_row32(void *c, int64_t ldc, int row, int col0, int n,
-                                            const float (&f)[32])
+__device__ __forceinline__ uint32_t pack2(float a, float b)
 {
     if constexpr (F16) {
-        __half *p = static_cast<__half *>(c) + static_cast<int64_t>(row) * ldc + col0;
-        if (col0 + 32 <= n && (reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint4 w;
-                __half2 h0 = __floats2half2_rn(f[8 * q + 0], f[8 * q + 1]);
-                __half2 h1 = __floats2half2_rn(f[8 * q + 2], f[8 * q + 3]);
-                __half2 h2 = __floats2half2_rn(f[8 * q + 4], f[8 * q + 5]);
-                __half2 h3 = __floats2half2_rn(f[8 * q + 6], f[8 * q + 7]);
-                w.x = *reinterpret_cast<uint32_t *>(&h0);
-                w.y = *reinterpret_cast<uint32_t *>(&h1);
-                w.z = *reinterpret_cast<uint32_t *>(&h2);
-                w.w = *reinterpret_cast<uint32_t *>(&h3);
-                reinterpret_cast<uint4 *>(p)[q] = w;
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (col0 + j < n) p[j] = __float2half_rn(f[j]);
-        }
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&h);
     } else {
-        __nv_bfloat16 *p = static_cast<__nv_bfloat16 *>(c) + static_cast<int64_t>(row) * ldc + col0;
-        if (col0 + 32 <= n && (reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint4 w;
-                __nv_bfloat162 h0 = __floats2bfloat162_rn(f[8 * q + 0], f[8 * q + 1]);
-                __nv_bfloat162 h1 = __floats2bfloat162_rn(f[8 * q + 2], f[8 * q + 3]);
-                __nv_bfloat162 h2 = __floats2bfloat162_rn(f[8 * q + 4], f[8 * q + 5]);
-                __nv_bfloat162 h3 = __floats2bfloat162_rn(f[8 * q + 6], f[8 * q + 7]);
-                w.x = *reinterpret_cast<uint32_t *>(&h0);
-                w.y = *reinterpret_cast<uint32_t *>(&h1);
-                w.z = *reinterpret_cast<uint32_t *>(&h2);
-                w.w = *reinterpret_cast<uint32_t *>(&h3);
-                reinterpret_cast<uint4 *>(p)[q] = w;
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (col0 + j < n) p[j] = __float2bfloat16_rn(f[j]);
-        }
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&h);
     }
 }
 
+// Stores 32 consecutive 16-bit C values of one row (16 packed pairs) at
+// (row, col0), clipped at column n; 16-byte vector stores when aligned.
+__device__ __forceinline__ void store_packed32(void *c, int64_t ldc, int row, int col0, int n, const uint32_t (&w)[16])
+{
+    uint16_t *p = static_cast<uint16_t *>(c) + static_cast<int64_t>(row) * ldc + col0;
+    if (col0 + 32 <= n && (reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
+        uint4 *q = reinterpret_cast<uint4 *>(p);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) q[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (col0 + j < n) p[j] = static_cast<uint16_t>((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu));
+    }
+}
+
+__device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// One unit of work: an output tile, or one K-split of it.
+struct Unit {
+    int g, tile, m_tile, n_tile, split, s_begin, nst;
+};
+
+template <int MAXG>
+__device__ __forceinline__ Unit decode_unit(const GemmParams<MAXG> &p, int u)
+{
+    Unit w;
+    w.tile = u % p.total_tiles;
+    w.split = u / p.total_tiles;
+    int g = 0;
+#pragma unroll 1
+    while (g + 1 < p.num_groups && w.tile >= p.prob[g + 1].tile_start) ++g;
+    w.g = g;
+    const GemmProblemDev &pr = p.prob[g];
+    const int local = w.tile - pr.tile_start;
+    w.m_tile = local % pr.m_tiles;
+    w.n_tile = local / pr.m_tiles;
+    const int k_stages = (pr.k + 255) / 256;
+    w.s_begin = static_cast<int>(static_cast<int64_t>(k_stages) * w.split / p.splits);
+    w.nst = static_cast<int>(static_cast<int64_t>(k_stages) * (w.split + 1) / p.splits) - w.s_begin;
+    return w;
+}
+
+// Persistent block-scaled GEMM: each CTA loops over units blockIdx.x,
+// blockIdx.x + gridDim.x, ... Warp roles:
+//   warp 0 lane 0  TMA producer (stage ring shared by all units of the CTA)
+//   warp 1         TMEM owner; lane 0 issues the MMAs of every unit
+//   warp 2 lane 0  copies each stage's scale blocks smem -> TMEM
+//   warps 4-7      epilogue: drain the accumulator rows of a finished unit
+//                  into registers, hand TMEM back to the MMA issuer, then
+//                  write C while the next unit's mainloop runs
 template <int KIND, int BN, int STAGES, int MAXG, bool F16>
-__global__ void __launch_bounds__(128, 1) bs_gemm_kernel(const __grid_constant__ GemmParams<MAXG> p)
+__global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__ GemmParams<MAXG> p)
 {
     using Cfg = GemmCfg<KIND, BN, STAGES>;
     constexpr bool MX = Cfg::MX;
@@ -143,29 +157,16 @@ __global__ void __launch_bounds__(128, 1) bs_gemm_kernel(const __grid_constant__
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * Cfg::STAGE_BYTES);
     uint64_t *empty = full + STAGES;
     uint64_t *sf_full = empty + STAGES;   // [STAGES] the stage's scales are in TMEM
-    uint64_t *accf = sf_full + STAGES;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accf + 1);
+    uint64_t *accf = sf_full + STAGES;    // a unit's accumulator is complete
+    uint64_t *acc_empty = accf + 1;       // the epilogue has drained the accumulator
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 1);
     int *last_flag = reinterpret_cast<int *>(tmem_slot + 1);
-    int *abort_flag = last_flag + 1;
+    volatile int *abort_flag = last_flag + 1;
+    volatile int *epi_go = last_flag + 2;   // [2] per-unit decision of the epilogue warps
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-
-    // ---- tile decode: group by prefix sums, then m fastest within an n-tile
-    const int tile = blockIdx.x;
-    int g = 0;
-#pragma unroll 1
-    while (g + 1 < p.num_groups && tile >= p.prob[g + 1].tile_start) ++g;
-    const GemmProblemDev &pr = p.prob[g];
-    const int local = tile - pr.tile_start;
-    const int m_tile = local % pr.m_tiles;
-    const int n_tile = local / pr.m_tiles;
-    const int k_stages = (pr.k + 255) / 256;
-    const int split = blockIdx.y;
-    const int s_begin = static_cast<int>(static_cast<int64_t>(k_stages) * split / p.splits);
-    const int s_end = static_cast<int>(static_cast<int64_t>(k_stages) * (split + 1) / p.splits);
-    const int nst = s_end - s_begin;
-    const int k_steps_total = (pr.k + 63) / 64;
+    const int units = p.total_tiles * p.splits;
 
     if (threadIdx.x == 0) {
 #pragma unroll
@@ -175,181 +176,261 @@ __global__ void __launch_bounds__(128, 1) bs_gemm_kernel(const __grid_constant__
             mbar_init(sf_full + s, 1);
         }
         mbar_init(accf, 1);
+        mbar_init(acc_empty, 128);
         *abort_flag = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&p.tma[g]);
-        tma_prefetch_desc(&p.tmb[g]);
+        for (int g = 0; g < p.num_groups; ++g) {
+            tma_prefetch_desc(&p.tma[g]);
+            tma_prefetch_desc(&p.tmb[g]);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
         tmem_relinquish();
     }
+    // every global access waits for the preceding grid in the stream
+    grid_dependency_wait();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    grid_launch_dependents();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tmem_acc = tmem;
     const uint32_t tmem_sf = tmem + BN;
-    int issued = 0;  // stages armed by the producer (warp 0 lane 0 only)
+    int issued = 0;   // stages armed by the producer (warp 0 lane 0 only)
 
-    if (warp == 0 && lane == 0) {
-        // ------------------------------------------------------ TMA producer
-        const uint64_t pol = policy_evict_last();
-        int nch_valid = 0;
-#pragma unroll
-        for (int j = 0; j < Cfg::NCH; ++j)
-            if ((n_tile * Cfg::NCH + j) * 128 < pr.n) ++nch_valid;
-        for (int i = 0; i < nst; ++i) {
-            const int slot = i % STAGES;
-            if (i >= STAGES && !mbar_wait(empty + slot, ((i / STAGES) - 1) & 1, &g_gemm_error, kErrWaitEmpty)) {
-                *abort_flag = 1;
-                break;
-            }
-            const int ks = s_begin + i;
-            uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
-            const int blk0 = ks * Cfg::SF_BLK;
-            const int nblk = min(Cfg::SF_BLK, pr.sf_cblocks - blk0);
-            const uint32_t bytes = Cfg::A_BYTES + Cfg::B_BYTES + (1 + nch_valid) * nblk * 512;
-            mbar_arrive_expect_tx(full + slot, bytes);
-            tma_load_2d(st, &p.tma[g], ks * 128, m_tile * 128, full + slot, pol);
-            tma_load_2d(st + Cfg::A_BYTES, &p.tmb[g], ks * 128, n_tile * BN, full + slot, pol);
-            bulk_load(st + Cfg::A_BYTES + Cfg::B_BYTES,
-                      pr.sfa + (static_cast<size_t>(m_tile) * pr.sf_cblocks + blk0) * 512, nblk * 512,
-                      full + slot, pol);
-            for (int j = 0; j < nch_valid; ++j)
-                bulk_load(st + Cfg::A_BYTES + Cfg::B_BYTES + Cfg::SFA_BYTES + j * Cfg::SF_BLK * 512,
-                          pr.sfb + (static_cast<size_t>(n_tile * Cfg::NCH + j) * pr.sf_cblocks + blk0) * 512,
-                          nblk * 512, full + slot, pol);
-            issued = i + 1;
-        }
-    } else if (warp == 1 && lane == 0) {
-        // ------------------------------------------------------- MMA issuer
-        // Only MMAs are issued here (each tcgen05 instruction costs tens of
-        // cycles to issue); warp 2 stages the scale factors into TMEM.
-        constexpr uint32_t IDESC = idesc_block_scaled(BN, MX);
-        for (int i = 0; i < nst; ++i) {
-            const int slot = i % STAGES;
-            if (!mbar_wait(full + slot, (i / STAGES) & 1, &g_gemm_error, kErrWaitFull) ||
-                !mbar_wait(sf_full + slot, (i / STAGES) & 1, &g_gemm_error, kErrWaitFull)) {
-                *abort_flag = 1;
-                break;
-            }
-            tc_fence_after();
-            uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
-            const uint32_t a_base = smem_u32(st);
-            const uint32_t b_base = smem_u32(st + Cfg::A_BYTES);
-            const uint32_t tsfa = tmem_sf + slot * Cfg::SF_COLS;
-            const uint32_t tsfb = tsfa + Cfg::SF_COLS_A;
-            const int ks = s_begin + i;
-            const int ksteps = min(4, k_steps_total - ks * 4);
-            for (int kk = 0; kk < ksteps; ++kk) {
-                const uint64_t ad = sdesc_sw128(a_base + kk * 32);
-                const uint64_t bd = sdesc_sw128(b_base + kk * 32);
-                const int blk = MX ? kk / 2 : kk;
-                const uint32_t sfid = MX ? static_cast<uint32_t>(kk & 1) * 2u : 0u;
-                const uint32_t idesc = idesc_with_sf_ids(IDESC, sfid, sfid);
-                const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-                if constexpr (MX)
-                    mma_mxf4(tmem_acc, ad, bd, idesc, tsfa + blk * 4, tsfb + blk * Cfg::NCH * 4, acc);
-                else
-                    mma_nvf4(tmem_acc, ad, bd, idesc, tsfa + blk * 4, tsfb + blk * Cfg::NCH * 4, acc);
-            }
-            tc_commit(empty + slot);
-        }
-        // arrives once every MMA issued above has completed (also on abort)
-        tc_commit(accf);
-    } else if (warp == 2 && lane == 0) {
-        // ------------------------------------- scale staging, smem -> TMEM
-        // A stage's TMEM scale slot is rewritten only after the stage that
-        // used it has been consumed: its smem slot was refilled, which needed
-        // the MMAs' "empty" commit, so the full wait below orders the copies.
-        for (int i = 0; i < nst; ++i) {
-            const int slot = i % STAGES;
-            if (!mbar_wait(full + slot, (i / STAGES) & 1, &g_gemm_error, kErrWaitFull)) {
-                *abort_flag = 1;
-                break;
-            }
-            tc_fence_after();
-            uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
-            const uint32_t sfa_s = smem_u32(st + Cfg::A_BYTES + Cfg::B_BYTES);
-            const uint32_t sfb_s = sfa_s + Cfg::SFA_BYTES;
-            const uint32_t tsfa = tmem_sf + slot * Cfg::SF_COLS;
-            const uint32_t tsfb = tsfa + Cfg::SF_COLS_A;
-            const int ks = s_begin + i;
-            const int ksteps = min(4, k_steps_total - ks * 4);
-            const int nblk = MX ? (ksteps + 1) / 2 : ksteps;
-            for (int b = 0; b < nblk; ++b) {
-                tc_cp_scale_block(tsfa + b * 4, sdesc_scale(sfa_s + b * 512));
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------------ TMA producer
+            const uint64_t pol = policy_evict_last();
+            int gs = 0;
+            for (int u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
+                const Unit w = decode_unit(p, u);
+                const GemmProblemDev &pr = p.prob[w.g];
+                int nch_valid = 0;
 #pragma unroll
                 for (int j = 0; j < Cfg::NCH; ++j)
-                    tc_cp_scale_block(tsfb + (b * Cfg::NCH + j) * 4,
-                                      sdesc_scale(sfb_s + (j * Cfg::SF_BLK + b) * 512));
+                    if ((w.n_tile * Cfg::NCH + j) * 128 < pr.n) ++nch_valid;
+                for (int i = 0; i < w.nst; ++i, ++gs) {
+                    const int slot = gs % STAGES;
+                    if (gs >= STAGES &&
+                        !mbar_wait(empty + slot, ((gs / STAGES) - 1) & 1, &g_gemm_error, kErrWaitEmpty)) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    const int ks = w.s_begin + i;
+                    uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
+                    const int blk0 = ks * Cfg::SF_BLK;
+                    const int nblk = min(Cfg::SF_BLK, pr.sf_cblocks - blk0);
+                    const uint32_t bytes = Cfg::A_BYTES + Cfg::B_BYTES + (1 + nch_valid) * nblk * 512;
+                    mbar_arrive_expect_tx(full + slot, bytes);
+                    tma_load_2d(st, &p.tma[w.g], ks * 128, w.m_tile * 128, full + slot, pol);
+                    tma_load_2d(st + Cfg::A_BYTES, &p.tmb[w.g], ks * 128, w.n_tile * BN, full + slot, pol);
+                    bulk_load(st + Cfg::A_BYTES + Cfg::B_BYTES,
+                              pr.sfa + (static_cast<size_t>(w.m_tile) * pr.sf_cblocks + blk0) * 512, nblk * 512,
+                              full + slot, pol);
+                    for (int j = 0; j < nch_valid; ++j)
+                        bulk_load(st + Cfg::A_BYTES + Cfg::B_BYTES + Cfg::SFA_BYTES + j * Cfg::SF_BLK * 512,
+                                  pr.sfb + (static_cast<size_t>(w.n_tile * Cfg::NCH + j) * pr.sf_cblocks + blk0) * 512,
+                                  nblk * 512, full + slot, pol);
+                    issued = gs + 1;
+                }
             }
-            tc_commit(sf_full + slot);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // -------------------------------------------------------- MMA issuer
+            // Only MMAs are issued here (a tcgen05 instruction costs tens of
+            // cycles to issue); warp 2 stages the scale factors into TMEM.
+            constexpr uint32_t IDESC = idesc_block_scaled(BN, MX);
+            int gs = 0, ul = 0, commits = 0;
+            for (int u = blockIdx.x; u < units; u += gridDim.x, ++ul) {
+                const Unit w = decode_unit(p, u);
+                const GemmProblemDev &pr = p.prob[w.g];
+                const int k_steps_total = (pr.k + 63) / 64;
+                if (ul > 0 && !mbar_wait(acc_empty, (ul - 1) & 1, &g_gemm_error, kErrWaitAccum)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                tc_fence_after();
+                bool ok = true;
+                for (int i = 0; i < w.nst; ++i, ++gs) {
+                    const int slot = gs % STAGES;
+                    const uint32_t ph = (gs / STAGES) & 1;
+                    if (!mbar_wait(full + slot, ph, &g_gemm_error, kErrWaitFull) ||
+                        !mbar_wait(sf_full + slot, ph, &g_gemm_error, kErrWaitFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
+                    const uint32_t a_base = smem_u32(st);
+                    const uint32_t b_base = smem_u32(st + Cfg::A_BYTES);
+                    const uint32_t tsfa = tmem_sf + slot * Cfg::SF_COLS;
+                    const uint32_t tsfb = tsfa + Cfg::SF_COLS_A;
+                    const int ks = w.s_begin + i;
+                    const int ksteps = min(4, k_steps_total - ks * 4);
+                    for (int kk = 0; kk < ksteps; ++kk) {
+                        const uint64_t ad = sdesc_sw128(a_base + kk * 32);
+                        const uint64_t bd = sdesc_sw128(b_base + kk * 32);
+                        const int blk = MX ? kk / 2 : kk;
+                        const uint32_t sfid = MX ? static_cast<uint32_t>(kk & 1) * 2u : 0u;
+                        const uint32_t idesc = idesc_with_sf_ids(IDESC, sfid, sfid);
+                        const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                        if constexpr (MX)
+                            mma_mxf4(tmem_acc, ad, bd, idesc, tsfa + blk * 4, tsfb + blk * Cfg::NCH * 4, acc);
+                        else
+                            mma_nvf4(tmem_acc, ad, bd, idesc, tsfa + blk * 4, tsfb + blk * Cfg::NCH * 4, acc);
+                    }
+                    tc_commit(empty + slot);
+                }
+                // arrives once every MMA issued above has completed (also on abort)
+                tc_commit(accf);
+                ++commits;
+                if (!ok) {
+                    *abort_flag = 1;
+                    break;
+                }
+            }
+            // The epilogue waits for every commit unless it stopped early; the
+            // accumulator must not be in use when TMEM is released.
+            if (commits > 0) mbar_wait(accf, (commits - 1) & 1, &g_gemm_error, kErrWaitDrain);
+        }
+    } else if (warp == 2) {
+        if (lane == 0) {
+            // ----------------------------------------- scale staging, smem -> TMEM
+            // A stage's TMEM scale slot is rewritten only after the stage that
+            // used it has been consumed: its smem slot was refilled, which needed
+            // the MMAs' "empty" commit, so the full wait below orders the copies.
+            int gs = 0;
+            for (int u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
+                const Unit w = decode_unit(p, u);
+                const GemmProblemDev &pr = p.prob[w.g];
+                const int k_steps_total = (pr.k + 63) / 64;
+                for (int i = 0; i < w.nst; ++i, ++gs) {
+                    const int slot = gs % STAGES;
+                    if (!mbar_wait(full + slot, (gs / STAGES) & 1, &g_gemm_error, kErrWaitFull)) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
+                    const uint32_t sfa_s = smem_u32(st + Cfg::A_BYTES + Cfg::B_BYTES);
+                    const uint32_t sfb_s = sfa_s + Cfg::SFA_BYTES;
+                    const uint32_t tsfa = tmem_sf + slot * Cfg::SF_COLS;
+                    const uint32_t tsfb = tsfa + Cfg::SF_COLS_A;
+                    const int ks = w.s_begin + i;
+                    const int ksteps = min(4, k_steps_total - ks * 4);
+                    const int nblk = MX ? (ksteps + 1) / 2 : ksteps;
+                    for (int b = 0; b < nblk; ++b) {
+                        tc_cp_scale_block(tsfa + b * 4, sdesc_scale(sfa_s + b * 512));
+#pragma unroll
+                        for (int j = 0; j < Cfg::NCH; ++j)
+                            tc_cp_scale_block(tsfb + (b * Cfg::NCH + j) * 4,
+                                              sdesc_scale(sfb_s + (j * Cfg::SF_BLK + b) * 512));
+                    }
+                    tc_commit(sf_full + slot);
+                }
+            }
+            // scale copies still in flight (only after an abort) finish before TMEM is released
+            for (int i = max(0, gs - STAGES); i < gs; ++i)
+                mbar_wait(sf_full + (i % STAGES), (i / STAGES) & 1, &g_gemm_error, kErrWaitDrain);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;                  // TMEM lane quadrant of this warp
+        const int row_in_tile = q * 32 + lane;
+        const uint32_t t_row = tmem_acc + (static_cast<uint32_t>(q * 32) << 16);
+        int ul = 0;
+        for (int u = blockIdx.x; u < units; u += gridDim.x, ++ul) {
+            const Unit w = decode_unit(p, u);
+            const GemmProblemDev &pr = p.prob[w.g];
+            // one thread waits and decides for all four warps, so that they
+            // leave the loop together (the split-K path has named barriers)
+            if (threadIdx.x == 128) {
+                const bool ok = mbar_wait(accf, ul & 1, &g_gemm_error, kErrWaitAccum);
+                if (!ok) *abort_flag = 1;
+                epi_go[ul & 1] = ok;
+            }
+            epilogue_bar();
+            if (!epi_go[ul & 1]) break;
+            tc_fence_after();
+            const bool run = (*abort_flag == 0);
+            const int row = w.m_tile * 128 + row_in_tile;
+            if (p.splits == 1) {
+                // drain the row into registers, release TMEM, then store
+                uint32_t pk[BN / 2];
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(t_row + c * 32, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        pk[c * 16 + j] = pack2<F16>(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                }
+                tc_fence_before();
+                mbar_arrive(acc_empty);
+                if (run && row < pr.m) {
+#pragma unroll
+                    for (int c = 0; c < BN / 32; ++c) {
+                        const int col0 = w.n_tile * BN + c * 32;
+                        if (col0 < pr.n) {
+                            uint32_t part[16];
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) part[j] = pk[c * 16 + j];
+                            store_packed32(pr.c, pr.ldc, row, col0, pr.n, part);
+                        }
+                    }
+                }
+            } else {
+                // split-K: partials [split][n_tile][BN][M] fp32 (rows < M only),
+                // then the last split to arrive sums them in split order
+                const size_t col_stride = static_cast<size_t>(pr.m);
+                float *part = p.partials + (static_cast<size_t>(w.split) * pr.n_tiles + w.n_tile) * BN * col_stride;
+                for (int c0 = 0; c0 < BN; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(t_row + c0, v);
+                    tmem_ld_wait();
+                    if (run && row < pr.m) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) part[(c0 + j) * col_stride + row] = __uint_as_float(v[j]);
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(acc_empty);
+                __threadfence();
+                epilogue_bar();
+                if (threadIdx.x == 128) {
+                    const int old = atomicAdd(p.tickets + w.tile, 1);
+                    *last_flag = (old == p.splits - 1);
+                }
+                epilogue_bar();
+                if (run && *last_flag) {
+                    __threadfence();
+                    for (int c0 = 0; c0 < BN; c0 += 32) {
+                        const int col0 = w.n_tile * BN + c0;
+                        if (col0 >= pr.n || row >= pr.m) break;
+                        float f[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) f[j] = 0.0f;
+                        for (int sp = 0; sp < p.splits; ++sp) {
+                            const float *qv = p.partials + (static_cast<size_t>(sp) * pr.n_tiles + w.n_tile) * BN * col_stride;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) f[j] += __ldcg(qv + (c0 + j) * col_stride + row);
+                        }
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) pk[j] = pack2<F16>(f[2 * j], f[2 * j + 1]);
+                        store_packed32(pr.c, pr.ldc, row, col0, pr.n, pk);
+                    }
+                    if (threadIdx.x == 128) p.tickets[w.tile] = 0;
+                }
+                epilogue_bar();   // last_flag is reused by the next unit
+            }
         }
     }
     __syncwarp();
-
-    // ----------------------------------------------------------- epilogue
-    const bool acc_ok = mbar_wait(accf, 0, &g_gemm_error, kErrWaitAccum);
-    tc_fence_after();
-    __syncthreads();
-    const bool run = acc_ok && (*abort_flag == 0);
-    const int row_in_tile = warp * 32 + lane;
-    const int row = m_tile * 128 + row_in_tile;
-    const uint32_t t_row = tmem_acc + (static_cast<uint32_t>(warp * 32) << 16);
-
-    if (run && p.splits == 1) {
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-            const int col0 = n_tile * BN + c0;
-            if (col0 >= pr.n) break;
-            uint32_t v[32];
-            tmem_ld32(t_row + c0, v);
-            tmem_ld_wait();
-            float f[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
-            if (row < pr.m) store_row32<F16>(pr.c, pr.ldc, row, col0, pr.n, f);
-        }
-    } else if (run) {
-        // partials: [split][n_tile][BN columns][M rows] fp32 (only rows < M),
-        // consecutive lanes = consecutive rows, so stores and loads coalesce
-        const size_t col_stride = static_cast<size_t>(pr.m);
-        float *part = p.partials + (static_cast<size_t>(split) * pr.n_tiles + n_tile) * BN * col_stride;
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(t_row + c0, v);
-            tmem_ld_wait();
-            if (row < pr.m) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) part[(c0 + j) * col_stride + row] = __uint_as_float(v[j]);
-            }
-        }
-        __threadfence();
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            const int old = atomicAdd(p.tickets + tile, 1);
-            *last_flag = (old == p.splits - 1);
-        }
-        __syncthreads();
-        if (*last_flag) {
-            __threadfence();
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                const int col0 = n_tile * BN + c0;
-                if (col0 >= pr.n || row >= pr.m) break;
-                float f[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) f[j] = 0.0f;
-                for (int sp = 0; sp < p.splits; ++sp) {
-                    const float *q = p.partials + (static_cast<size_t>(sp) * pr.n_tiles + n_tile) * BN * col_stride;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) f[j] += __ldcg(q + (c0 + j) * col_stride + row);
-                }
-                store_row32<F16>(pr.c, pr.ldc, row, col0, pr.n, f);
-            }
-            if (threadIdx.x == 0) p.tickets[tile] = 0;
-        }
-    }
 
     // ----------------------------------------------------------- teardown
     tc_fence_before();
@@ -366,22 +447,36 @@ __global__ void __launch_bounds__(128, 1) bs_gemm_kernel(const __grid_constant__
 }
 
 template <int KIND, int BN, int STAGES, int MAXG, bool F16>
-cudaError_t launch_bs_gemm(const GemmParams<MAXG> &params, int splits, cudaStream_t stream)
+cudaError_t launch_bs_gemm(const GemmParams<MAXG> &params, cudaStream_t stream)
 {
     using Cfg = GemmCfg<KIND, BN, STAGES>;
     auto kern = bs_gemm_kernel<KIND, BN, STAGES, MAXG, F16>;
     static uint64_t configured = 0;  // one bit per device; setting it twice is harmless
+    static int sms_of[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (!(configured & (1ull << (dev & 63)))) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
         if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&sms_of[dev & 63], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
         configured |= 1ull << (dev & 63);
     }
-    dim3 grid(params.total_tiles, splits, 1);
-    kern<<<grid, 128, Cfg::SMEM_BYTES, stream>>>(params);
-    return cudaGetLastError();
+    const int units = params.total_tiles * params.splits;
+    const int grid = min(units, max(1, sms_of[dev & 63]));
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, params);
 }
 
 constexpr int kMxBN = 256, kMxStages = 4;
@@ -424,7 +519,7 @@ cudaError_t launch_gemm_mx(const GemmProblemHost &prob, int splits, float *parti
     P.splits = splits;
     P.partials = partials;
     P.tickets = tickets;
-    return launch_bs_gemm<0, kMxBN, kMxStages, 1, false>(P, splits, stream);
+    return launch_bs_gemm<0, kMxBN, kMxStages, 1, false>(P, stream);
 }
 
 cudaError_t launch_gemm_nv_grouped(const GemmProblemHost *probs, int num_groups, cudaStream_t stream)
@@ -438,7 +533,7 @@ cudaError_t launch_gemm_nv_grouped(const GemmProblemHost *probs, int num_groups,
     P.splits = 1;
     P.partials = nullptr;
     P.tickets = nullptr;
-    return launch_bs_gemm<1, kNvBN, kNvStages, kMaxGroups, true>(P, 1, stream);
+    return launch_bs_gemm<1, kNvBN, kNvStages, kMaxGroups, true>(P, stream);
 }
 
 int read_and_clear_gemm_error()
