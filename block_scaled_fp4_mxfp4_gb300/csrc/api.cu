@@ -179,6 +179,7 @@ size_t sf_bytes(int64_t rows, int64_t k, int vec)
 }
 
 struct GemmPlan {
+    int bn;        // tile width along N: 256, or 128 when 256-wide tiles leave most SMs idle
     int splits;
     int tiles;
     int n_tiles;
@@ -186,9 +187,10 @@ struct GemmPlan {
 
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K)
 {
-    const int bn = gemm_block_n(false);
     GemmPlan p;
     const int64_t m_tiles = (M + 127) / 128;
+    p.bn = 2 * m_tiles * ((N + 255) / 256) <= kPlanSms ? 128 : 256;
+    const int bn = p.bn;
     p.n_tiles = static_cast<int>((N + bn - 1) / bn);
     p.tiles = static_cast<int>(m_tiles * p.n_tiles);
     const int64_t k_stages = (K + 255) / 256;
@@ -215,7 +217,7 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K)
     WsLayout w;
     w.ldq = ((K / 2) + 15) / 16 * 16;
     const GemmPlan gp = plan_gemm(M, N, K);
-    const int bn = gemm_block_n(false);
+    const int bn = gp.bn;
     w.aq_off = 0;
     w.sf_off = up256(static_cast<size_t>(M) * w.ldq);
     w.part_off = w.sf_off + up256(sf_bytes(M, K, 32));
@@ -234,7 +236,8 @@ mxfp4_status_t run_gemm(const void *Aq, int64_t ldaq, const void *A_sf, const vo
     memset(&h, 0, sizeof(h));
     mxfp4_status_t st = fp4_map(Aq, K / 2, M, ldaq, 128, &h.tma);
     if (st != MXFP4_OK) return st;
-    st = fp4_map(Bq, K / 2, N, ldbq, gemm_block_n(false), &h.tmb);
+    const GemmPlan gp = plan_gemm(M, N, K);
+    st = fp4_map(Bq, K / 2, N, ldbq, gp.bn, &h.tmb);
     if (st != MXFP4_OK) return st;
     h.sfa = static_cast<const uint8_t *>(A_sf);
     h.sfb = static_cast<const uint8_t *>(B_sf);
@@ -243,11 +246,10 @@ mxfp4_status_t run_gemm(const void *Aq, int64_t ldaq, const void *A_sf, const vo
     h.m = static_cast<int>(M);
     h.n = static_cast<int>(N);
     h.k = static_cast<int>(K);
-    const GemmPlan gp = plan_gemm(M, N, K);
     uint8_t *w = static_cast<uint8_t *>(ws);
     float *part = gp.splits > 1 ? reinterpret_cast<float *>(w + wl.part_off) : nullptr;
     int *tickets = reinterpret_cast<int *>(w + wl.ticket_off);
-    return cuda_status(launch_gemm_mx(h, gp.splits, part, tickets, stream));
+    return cuda_status(launch_gemm_mx(h, gp.bn, gp.splits, part, tickets, stream));
 }
 
 }  // namespace
@@ -372,7 +374,7 @@ mxfp4_status_t nvfp4_group_gemm(const nvfp4_problem_t *problems, int num_groups,
     GemmProblemHost hp[kMaxGroups];
     memset(hp, 0, sizeof(hp));
     int64_t total_tiles = 0;
-    const int bn = gemm_block_n(true);
+    const int bn = gemm_block_n_nv();
     for (int g = 0; g < num_groups; ++g) {
         const nvfp4_problem_t &p = problems[g];
         if (!p.a || !p.sfa || !p.b || !p.sfb || !p.c) return MXFP4_ERR_INVALID_ARG;
@@ -470,7 +472,7 @@ mxfp4_status_t mxfp4_gemm_a4w4_noalloc(const void *Aq, int64_t ldaq, const void 
     memset(&wl, 0, sizeof(wl));
     size_t part = 0;
     if (gp.splits > 1)
-        part = static_cast<size_t>(gp.splits) * gp.n_tiles * gemm_block_n(false) * static_cast<size_t>(M) * 4;
+        part = static_cast<size_t>(gp.splits) * gp.n_tiles * gp.bn * static_cast<size_t>(M) * 4;
     wl.part_off = 0;
     wl.ticket_off = up256(part);
     wl.total = wl.ticket_off + up256(static_cast<size_t>(gp.tiles) * 4);

@@ -479,7 +479,8 @@ cudaError_t launch_bs_gemm(const GemmParams<MAXG> &params, cudaStream_t stream)
     return cudaLaunchKernelEx(&cfg, kern, params);
 }
 
-constexpr int kMxBN = 256, kMxStages = 4;
+constexpr int kMxStages = 4;        // BN = 256
+constexpr int kMxNarrowStages = 6;  // BN = 128: 34 KB stages
 constexpr int kNvBN = 256, kNvStages = 4;
 
 template <int MAXG>
@@ -505,21 +506,23 @@ void fill_problem(GemmParams<MAXG> &P, int g, const GemmProblemHost &h, int bn, 
 
 }  // namespace
 
-int gemm_block_n(bool nvfp4) { return nvfp4 ? kNvBN : kMxBN; }
+int gemm_block_n_nv() { return kNvBN; }
 
-cudaError_t launch_gemm_mx(const GemmProblemHost &prob, int splits, float *partials, int *tickets,
+cudaError_t launch_gemm_mx(const GemmProblemHost &prob, int bn, int splits, float *partials, int *tickets,
                            cudaStream_t stream)
 {
+    if (bn != 128 && bn != 256) return cudaErrorInvalidValue;
     GemmParams<1> P;
     memset(&P, 0, sizeof(P));
     int tiles = 0;
-    fill_problem(P, 0, prob, kMxBN, 32, tiles);
+    fill_problem(P, 0, prob, bn, 32, tiles);
     P.num_groups = 1;
     P.total_tiles = tiles;
     P.splits = splits;
     P.partials = partials;
     P.tickets = tickets;
-    return launch_bs_gemm<0, kMxBN, kMxStages, 1, false>(P, stream);
+    if (bn == 128) return launch_bs_gemm<0, 128, kMxNarrowStages, 1, false>(P, stream);
+    return launch_bs_gemm<0, 256, kMxStages, 1, false>(P, stream);
 }
 
 cudaError_t launch_gemm_nv_grouped(const GemmProblemHost *probs, int num_groups, cudaStream_t stream)

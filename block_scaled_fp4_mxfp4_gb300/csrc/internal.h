@@ -28,12 +28,13 @@ struct GemmProblemHost {
     int m, n, k;
 };
 
-// Tile width along N used by the MXFP4 / NVFP4 GEMM kernels (box rows of tmb).
-int gemm_block_n(bool nvfp4);
+// Tile width along N of the grouped NVFP4 GEMM (box rows of tmb).
+int gemm_block_n_nv();
 
-// MXFP4 (kind::mxf4, bf16 C). splits > 1 needs `partials` (splits*tiles*bn*128
-// floats) and zeroed `tickets` (tiles ints).
-cudaError_t launch_gemm_mx(const GemmProblemHost &prob, int splits, float *partials,
+// MXFP4 (kind::mxf4, bf16 C) with tiles of 128 x bn, bn = 128 or 256 (the box
+// rows of prob.tmb). splits > 1 needs `partials` (splits * n_tiles * bn * M
+// floats) and zeroed `tickets` (one int per tile).
+cudaError_t launch_gemm_mx(const GemmProblemHost &prob, int bn, int splits, float *partials,
                            int *tickets, cudaStream_t stream);
 // Grouped NVFP4 (kind::mxf4nvf4, fp16 C), one launch over all groups.
 cudaError_t launch_gemm_nv_grouped(const GemmProblemHost *probs, int num_groups,
