@@ -165,7 +165,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    grid_launch_dependents();
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
@@ -275,6 +274,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int nacc = min(nst, kStageWarps);       // accumulators that hold data
     if (warp >= 2) {
         const bool acc_ok = mbar_wait(accf, 0, &g_fused_error, kErrWaitAccum);
+        // The next grid in the stream may start once the accumulators are
+        // complete. Its weight stream then overlaps this grid's reduction and
+        // exit instead of competing with this grid's loads of A (measured on
+        // the 16 x 2112 x 7168 workload: 6.65 -> 6.13 us per call, against a
+        // trigger right after the dependency wait).
+        grid_launch_dependents();
         tc_fence_after();
         const int q = warp & 3;                      // TMEM lane quadrant of this warp
         const int n_local = q * 32 + lane;

@@ -82,6 +82,8 @@ struct GemmCfg {
     static_assert(STAGE_BYTES % 1024 == 0, "stage must keep 1024-byte alignment");
     static_assert(BN + STAGES * SF_COLS <= 512, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    // full, empty, sf_full, sf_data per stage; accf, acc_empty; TMEM address and flags
+    static_assert((4 * STAGES + 2) * 8 + 16 <= BAR_BYTES, "barrier area");
 };
 
 template <bool F16>
@@ -157,7 +159,8 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * Cfg::STAGE_BYTES);
     uint64_t *empty = full + STAGES;
     uint64_t *sf_full = empty + STAGES;   // [STAGES] the stage's scales are in TMEM
-    uint64_t *accf = sf_full + STAGES;    // a unit's accumulator is complete
+    uint64_t *sf_data = sf_full + STAGES; // [STAGES] the stage's scale bytes are in smem
+    uint64_t *accf = sf_data + STAGES;    // a unit's accumulator is complete
     uint64_t *acc_empty = accf + 1;       // the epilogue has drained the accumulator
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 1);
     int *last_flag = reinterpret_cast<int *>(tmem_slot + 1);
@@ -174,6 +177,7 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
             mbar_init(full + s, 1);
             mbar_init(empty + s, 1);
             mbar_init(sf_full + s, 1);
+            mbar_init(sf_data + s, 1);
         }
         mbar_init(accf, 1);
         mbar_init(acc_empty, 128);
@@ -222,17 +226,19 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
                     uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
                     const int blk0 = ks * Cfg::SF_BLK;
                     const int nblk = min(Cfg::SF_BLK, pr.sf_cblocks - blk0);
-                    const uint32_t bytes = Cfg::A_BYTES + Cfg::B_BYTES + (1 + nch_valid) * nblk * 512;
-                    mbar_arrive_expect_tx(full + slot, bytes);
-                    tma_load_2d(st, &p.tma[w.g], ks * 128, w.m_tile * 128, full + slot, pol);
-                    tma_load_2d(st + Cfg::A_BYTES, &p.tmb[w.g], ks * 128, w.n_tile * BN, full + slot, pol);
+                    // the scale blocks first, on their own barrier: their copy into
+                    // TMEM then overlaps the arrival of the operand tiles
+                    mbar_arrive_expect_tx(sf_data + slot, (1 + nch_valid) * nblk * 512);
                     bulk_load(st + Cfg::A_BYTES + Cfg::B_BYTES,
                               pr.sfa + (static_cast<size_t>(w.m_tile) * pr.sf_cblocks + blk0) * 512, nblk * 512,
-                              full + slot, pol);
+                              sf_data + slot, pol);
                     for (int j = 0; j < nch_valid; ++j)
                         bulk_load(st + Cfg::A_BYTES + Cfg::B_BYTES + Cfg::SFA_BYTES + j * Cfg::SF_BLK * 512,
                                   pr.sfb + (static_cast<size_t>(w.n_tile * Cfg::NCH + j) * pr.sf_cblocks + blk0) * 512,
-                                  nblk * 512, full + slot, pol);
+                                  nblk * 512, sf_data + slot, pol);
+                    mbar_arrive_expect_tx(full + slot, Cfg::A_BYTES + Cfg::B_BYTES);
+                    tma_load_2d(st, &p.tma[w.g], ks * 128, w.m_tile * 128, full + slot, pol);
+                    tma_load_2d(st + Cfg::A_BYTES, &p.tmb[w.g], ks * 128, w.n_tile * BN, full + slot, pol);
                     issued = gs + 1;
                 }
             }
@@ -301,7 +307,8 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
             // ----------------------------------------- scale staging, smem -> TMEM
             // A stage's TMEM scale slot is rewritten only after the stage that
             // used it has been consumed: its smem slot was refilled, which needed
-            // the MMAs' "empty" commit, so the full wait below orders the copies.
+            // the MMAs' "empty" commit, so the scale-data wait below orders the
+            // copies.
             int gs = 0;
             for (int u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
                 const Unit w = decode_unit(p, u);
@@ -309,7 +316,7 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
                 const int k_steps_total = (pr.k + 63) / 64;
                 for (int i = 0; i < w.nst; ++i, ++gs) {
                     const int slot = gs % STAGES;
-                    if (!mbar_wait(full + slot, (gs / STAGES) & 1, &g_gemm_error, kErrWaitFull)) {
+                    if (!mbar_wait(sf_data + slot, (gs / STAGES) & 1, &g_gemm_error, kErrWaitFull)) {
                         *abort_flag = 1;
                         break;
                     }
@@ -437,8 +444,10 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
     __syncthreads();
     if (warp == 0 && lane == 0) {
         // copies still in flight (only after an abort) must land before exit
-        for (int i = max(0, issued - STAGES); i < issued; ++i)
+        for (int i = max(0, issued - STAGES); i < issued; ++i) {
+            mbar_wait(sf_data + (i % STAGES), (i / STAGES) & 1, &g_gemm_error, kErrWaitDrain);
             mbar_wait(full + (i % STAGES), (i / STAGES) & 1, &g_gemm_error, kErrWaitDrain);
+        }
     }
     if (warp == 1) {
         tc_fence_after();
