@@ -145,7 +145,8 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams<MAXG> &p, int u)
 // blockIdx.x + gridDim.x, ... Warp roles:
 //   warp 0 lane 0  TMA producer (stage ring shared by all units of the CTA)
 //   warp 1         TMEM owner; lane 0 issues the MMAs of every unit
-//   warp 2 lane 0  copies each stage's scale blocks smem -> TMEM
+//   warps 2, 3     lane 0 of each copies half of each stage's scale blocks
+//                  smem -> TMEM
 //   warps 4-7      epilogue: drain the accumulator rows of a finished unit
 //                  into registers, hand TMEM back to the MMA issuer, then
 //                  write C while the next unit's mainloop runs
@@ -176,7 +177,7 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full + s, 1);
             mbar_init(empty + s, 1);
-            mbar_init(sf_full + s, 1);
+            mbar_init(sf_full + s, 2);   // one commit from each scale-copy thread
             mbar_init(sf_data + s, 1);
         }
         mbar_init(accf, 1);
@@ -247,7 +248,7 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
         if (lane == 0) {
             // -------------------------------------------------------- MMA issuer
             // Only MMAs are issued here (a tcgen05 instruction costs tens of
-            // cycles to issue); warp 2 stages the scale factors into TMEM.
+            // cycles to issue); warps 2 and 3 stage the scale factors into TMEM.
             constexpr uint32_t IDESC = idesc_block_scaled(BN, MX);
             int gs = 0, ul = 0, commits = 0;
             for (int u = blockIdx.x; u < units; u += gridDim.x, ++ul) {
@@ -302,9 +303,12 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
             // accumulator must not be in use when TMEM is released.
             if (commits > 0) mbar_wait(accf, (commits - 1) & 1, &g_gemm_error, kErrWaitDrain);
         }
-    } else if (warp == 2) {
+    } else if (warp == 2 || warp == 3) {
         if (lane == 0) {
             // ----------------------------------------- scale staging, smem -> TMEM
+            // Lane 0 of warps 2 and 3 share the copies of each stage (even and odd
+            // K blocks): one tcgen05.cp takes tens of cycles to issue, and a
+            // stage of NVFP4 scales needs twelve.
             // A stage's TMEM scale slot is rewritten only after the stage that
             // used it has been consumed: its smem slot was refilled, which needed
             // the MMAs' "empty" commit, so the scale-data wait below orders the
@@ -329,7 +333,7 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
                     const int ks = w.s_begin + i;
                     const int ksteps = min(4, k_steps_total - ks * 4);
                     const int nblk = MX ? (ksteps + 1) / 2 : ksteps;
-                    for (int b = 0; b < nblk; ++b) {
+                    for (int b = warp - 2; b < nblk; b += 2) {
                         tc_cp_scale_block(tsfa + b * 4, sdesc_scale(sfa_s + b * 512));
 #pragma unroll
                         for (int j = 0; j < Cfg::NCH; ++j)
