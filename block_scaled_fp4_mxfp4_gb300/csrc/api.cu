@@ -70,7 +70,7 @@ bool encoder()
 struct MapKey {
     uintptr_t ptr;
     int64_t inner, rows, stride;
-    int box_rows, dev, kind;   // kind 0: packed FP4 (u8, 128B swizzle)
+    int box_rows, dev, kind;   // kind 0: packed FP4 (u8, 128B swizzle); 1: scale blocks (u32)
     bool operator==(const MapKey &o) const
     {
         return ptr == o.ptr && inner == o.inner && rows == o.rows && stride == o.stride &&
@@ -135,6 +135,17 @@ mxfp4_status_t fp4_map(const void *base, int64_t inner, int64_t rows, int64_t st
                       CU_TENSOR_MAP_SWIZZLE_128B, out);
 }
 
+// Tensor map of a blocked scale buffer viewed as [blocks, 128 u32] (one
+// 512-byte block per row), box {128, box_blocks}: box_blocks consecutive
+// K-blocks of one 128-row chunk in one copy; zero fill past the last block.
+mxfp4_status_t sf_map(const void *base, int64_t blocks, int box_blocks, CUtensorMap *out)
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    MapKey key{reinterpret_cast<uintptr_t>(base), 128, blocks, 512, box_blocks, dev, 1};
+    return cached_map(key, base, CU_TENSOR_MAP_DATA_TYPE_UINT32, 128u, 128u, CU_TENSOR_MAP_SWIZZLE_NONE, out);
+}
+
 // ------------------------------------------------------------- validation
 inline bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool al4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -179,15 +190,29 @@ size_t sf_bytes(int64_t rows, int64_t k, int vec)
 }
 
 struct GemmPlan {
-    int bn;        // tile width along N: 256, or 128 when 256-wide tiles leave most SMs idle
+    bool pair;     // CTA-pair kernel (256 x 256 tiles); else single-CTA 128 x bn tiles
+    int bn;        // single-CTA tile width along N: 256, or 128 when 256-wide tiles leave
+                   // most SMs idle (and the B box rows: 128 for the pair kernel)
     int splits;
     int tiles;
     int n_tiles;
 };
 
+// The pair kernel needs at least one 256 x 256 tile per SM pair.
+bool use_pair(int64_t pair_tile_count) { return pair_tile_count >= kPlanSms / 2; }
+
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K)
 {
     GemmPlan p;
+    if (use_pair(pair_tiles(M, N))) {
+        p.pair = true;
+        p.bn = 128;
+        p.splits = 1;
+        p.tiles = pair_tiles(M, N);
+        p.n_tiles = static_cast<int>((N + 255) / 256);
+        return p;
+    }
+    p.pair = false;
     const int64_t m_tiles = (M + 127) / 128;
     p.bn = 2 * m_tiles * ((N + 255) / 256) <= kPlanSms ? 128 : 256;
     const int bn = p.bn;
@@ -249,6 +274,13 @@ mxfp4_status_t run_gemm(const void *Aq, int64_t ldaq, const void *A_sf, const vo
     uint8_t *w = static_cast<uint8_t *>(ws);
     float *part = gp.splits > 1 ? reinterpret_cast<float *>(w + wl.part_off) : nullptr;
     int *tickets = reinterpret_cast<int *>(w + wl.ticket_off);
+    if (gp.pair) {
+        st = sf_map(A_sf, static_cast<int64_t>(sf_bytes(M, K, 32) / 512), 2, &h.tmsfa);
+        if (st != MXFP4_OK) return st;
+        st = sf_map(B_sf, static_cast<int64_t>(sf_bytes(N, K, 32) / 512), 2, &h.tmsfb);
+        if (st != MXFP4_OK) return st;
+        return cuda_status(launch_gemm_mx_pair(h, stream));
+    }
     return cuda_status(launch_gemm_mx(h, gp.bn, gp.splits, part, tickets, stream));
 }
 
@@ -373,7 +405,7 @@ mxfp4_status_t nvfp4_group_gemm(const nvfp4_problem_t *problems, int num_groups,
     if (num_groups > NVFP4_MAX_GROUPS) return MXFP4_ERR_UNSUPPORTED_SHAPE;
     GemmProblemHost hp[kMaxGroups];
     memset(hp, 0, sizeof(hp));
-    int64_t total_tiles = 0;
+    int64_t total_tiles = 0, total_pair_tiles = 0;
     const int bn = gemm_block_n_nv();
     for (int g = 0; g < num_groups; ++g) {
         const nvfp4_problem_t &p = problems[g];
@@ -385,8 +417,10 @@ mxfp4_status_t nvfp4_group_gemm(const nvfp4_problem_t *problems, int num_groups,
         if (p.lda % 16 != 0 || p.ldb % 16 != 0) return MXFP4_ERR_MISALIGNED;
         if (!al16(p.a) || !al16(p.sfa) || !al16(p.b) || !al16(p.sfb) || !al2(p.c)) return MXFP4_ERR_MISALIGNED;
         total_tiles += ((p.m + 127) / 128) * ((p.n + bn - 1) / bn);
+        total_pair_tiles += pair_tiles(p.m, p.n);
     }
     if (total_tiles > kMaxDim) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+    const bool pair = use_pair(total_pair_tiles);
     int sms = 0;
     mxfp4_status_t st = current_device(&sms);
     if (st != MXFP4_OK) return st;
@@ -394,8 +428,14 @@ mxfp4_status_t nvfp4_group_gemm(const nvfp4_problem_t *problems, int num_groups,
         const nvfp4_problem_t &p = problems[g];
         st = fp4_map(p.a, p.k / 2, p.m, p.lda, 128, &hp[g].tma);
         if (st != MXFP4_OK) return st;
-        st = fp4_map(p.b, p.k / 2, p.n, p.ldb, bn, &hp[g].tmb);
+        st = fp4_map(p.b, p.k / 2, p.n, p.ldb, pair ? 128 : bn, &hp[g].tmb);
         if (st != MXFP4_OK) return st;
+        if (pair) {
+            st = sf_map(p.sfa, static_cast<int64_t>(sf_bytes(p.m, p.k, 16) / 512), 4, &hp[g].tmsfa);
+            if (st != MXFP4_OK) return st;
+            st = sf_map(p.sfb, static_cast<int64_t>(sf_bytes(p.n, p.k, 16) / 512), 4, &hp[g].tmsfb);
+            if (st != MXFP4_OK) return st;
+        }
         hp[g].sfa = static_cast<const uint8_t *>(p.sfa);
         hp[g].sfb = static_cast<const uint8_t *>(p.sfb);
         hp[g].c = p.c;
@@ -404,6 +444,7 @@ mxfp4_status_t nvfp4_group_gemm(const nvfp4_problem_t *problems, int num_groups,
         hp[g].n = static_cast<int>(p.n);
         hp[g].k = static_cast<int>(p.k);
     }
+    if (pair) return cuda_status(launch_gemm_nv_grouped_pair(hp, num_groups, static_cast<cudaStream_t>(stream)));
     return cuda_status(launch_gemm_nv_grouped(hp, num_groups, static_cast<cudaStream_t>(stream)));
 }
 
@@ -413,8 +454,9 @@ mxfp4_status_t mxfp4_get_device_error(int *code)
     if (cudaDeviceSynchronize() != cudaSuccess) return MXFP4_ERR_CUDA;
     const int g = read_and_clear_gemm_error();
     const int f = read_and_clear_fused_error();
-    if (g < 0 || f < 0) return MXFP4_ERR_CUDA;
-    *code = g != 0 ? g : (f != 0 ? 16 + f : 0);
+    const int pg = read_and_clear_gemm_pair_error();
+    if (g < 0 || f < 0 || pg < 0) return MXFP4_ERR_CUDA;
+    *code = g != 0 ? g : (f != 0 ? 16 + f : (pg != 0 ? 32 + pg : 0));
     return MXFP4_OK;
 }
 

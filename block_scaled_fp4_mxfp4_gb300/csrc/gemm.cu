@@ -24,6 +24,7 @@
 // then resets its ticket so the workspace stays zeroed.
 #include <cstring>
 
+#include "gemm_common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -33,86 +34,7 @@ __device__ int g_gemm_error;
 
 namespace {
 
-struct GemmProblemDev {
-    const uint8_t *sfa;
-    const uint8_t *sfb;
-    void *c;
-    int64_t ldc;
-    int m, n, k;
-    int m_tiles, n_tiles;
-    int tile_start;
-    int sf_cblocks;   // column blocks of 4 scales per 128-row chunk
-    int pad_;
-};
-
-template <int MAXG>
-struct GemmParams {
-    CUtensorMap tma[MAXG];
-    CUtensorMap tmb[MAXG];
-    GemmProblemDev prob[MAXG];
-    int num_groups;
-    int total_tiles;
-    int splits;
-    int pad_;
-    float *partials;
-    int *tickets;
-};
-
-__host__ __device__ constexpr uint32_t pow2_cols(uint32_t n)
-{
-    return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : n <= 256 ? 256 : 512;
-}
-
-template <int KIND, int BN, int STAGES>
-struct GemmCfg {
-    static constexpr bool MX = KIND == 0;
-    static constexpr int SF_BLK = MX ? 2 : 4;   // 512-B scale blocks per 128 rows per stage
-    static constexpr int NCH = BN / 128;        // 128-row chunks of the B tile
-    static constexpr uint32_t A_BYTES = 128 * 128;
-    static constexpr uint32_t B_BYTES = BN * 128;
-    static constexpr uint32_t SFA_BYTES = SF_BLK * 512;
-    static constexpr uint32_t SFB_BYTES = NCH * SF_BLK * 512;
-    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-    static constexpr uint32_t SF_COLS_A = SF_BLK * 4;
-    static constexpr uint32_t SF_COLS_B = NCH * SF_BLK * 4;
-    static constexpr uint32_t SF_COLS = SF_COLS_A + SF_COLS_B;
-    static constexpr uint32_t TMEM_COLS = pow2_cols(BN + STAGES * SF_COLS);
-    static constexpr uint32_t BAR_BYTES = 256;
-    static constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
-    static_assert(STAGE_BYTES % 1024 == 0, "stage must keep 1024-byte alignment");
-    static_assert(BN + STAGES * SF_COLS <= 512, "TMEM budget");
-    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-    // full, empty, sf_full, sf_data per stage; accf, acc_empty; TMEM address and flags
-    static_assert((4 * STAGES + 2) * 8 + 16 <= BAR_BYTES, "barrier area");
-};
-
-template <bool F16>
-__device__ __forceinline__ uint32_t pack2(float a, float b)
-{
-    if constexpr (F16) {
-        __half2 h = __floats2half2_rn(a, b);
-        return *reinterpret_cast<uint32_t *>(&h);
-    } else {
-        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-        return *reinterpret_cast<uint32_t *>(&h);
-    }
-}
-
-// Stores 32 consecutive 16-bit C values of one row (16 packed pairs) at
-// (row, col0), clipped at column n; 16-byte vector stores when aligned.
-__device__ __forceinline__ void store_packed32(void *c, int64_t ldc, int row, int col0, int n, const uint32_t (&w)[16])
-{
-    uint16_t *p = static_cast<uint16_t *>(c) + static_cast<int64_t>(row) * ldc + col0;
-    if (col0 + 32 <= n && (reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
-        uint4 *q = reinterpret_cast<uint4 *>(p);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) q[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-    } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (col0 + j < n) p[j] = static_cast<uint16_t>((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu));
-    }
-}
+using namespace gemm_detail;
 
 __device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 

@@ -1,0 +1,487 @@
+// Block-scaled FP4 GEMM on CTA pairs (tcgen05 cta_group::2), for problems
+// with enough 256 x 256 output tiles to fill the GPU: the MXFP4 GEMM at large
+// M (kind::mxf4, bf16 C) and the grouped NVFP4 GEMM (kind::mxf4nvf4
+// scale_vec::4X, fp16 C).
+//
+// What it computes is the same as the single-CTA kernel in gemm.cu
+// (kernelbot-amd-mxfp4-mm-517169 docstring steps 3-4 and the gemm_a4w4 call;
+// kernelbot-nvfp4-group-gemm-496271 nvfp4_gemm_kernel and its loop over
+// problems). The difference is the MMA: one instruction of M = 256, N = 256,
+// K = 64 runs on the tensor cores of both SMs of a cluster pair. Each CTA
+// holds its own 128 rows of A and one half of the 256 rows of B, so an SM
+// receives 32 KB of operands per 256-deep K stage instead of the 48 KB a
+// single-CTA 128 x 256 tile needs for the same work, and one thread issues the
+// MMAs of two SMs.
+//
+// Persistent: cluster pair p walks the pair tiles p, p + pairs, ...
+//   warp 0 lane 0   (both CTAs) TMA producer for this CTA's A rows and B half,
+//                   its A scale blocks and the scale blocks of all 256 B rows;
+//                   the copies of both CTAs complete rank 0's barriers, which
+//                   rank 0 arms with the bytes of both
+//   warp 1          (both CTAs) allocates / frees the pair's TMEM; lane 0 of
+//                   rank 0 issues the MMAs
+//   warps 2, 3      lane 0 of rank 0 copies the stage's scale blocks into both
+//                   CTAs' TMEM (even / odd K blocks)
+//   warps 4-7       (both CTAs) epilogue: drain this CTA's accumulator rows,
+//                   hand TMEM back (arrive on rank 0's barrier), store C while
+//                   the next tile's mainloop runs
+// MMA completion is signalled to both CTAs by multicast commits. Every wait
+// on an mbarrier is bounded; a final cluster barrier keeps both CTAs alive
+// until neither can touch the other's shared memory, then the pair frees its
+// TMEM together.
+#include <cstring>
+
+#include "gemm_common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mxfp4 {
+
+__device__ int g_gemm_pair_error;
+
+namespace {
+
+using namespace gemm_detail;
+
+template <int KIND, int STAGES>
+struct PairCfg {
+    static constexpr bool MX = KIND == 0;
+    static constexpr int SF_BLK = MX ? 2 : 4;           // 512-B scale blocks per 128 rows per stage
+    static constexpr uint32_t A_BYTES = 128 * 128;      // this CTA's 128 rows x 256 FP4
+    static constexpr uint32_t B_BYTES = 128 * 128;      // this CTA's half of the 256 B rows
+    static constexpr uint32_t SFA_BYTES = SF_BLK * 512;
+    static constexpr uint32_t SFB_BYTES = 2 * SF_BLK * 512;   // both 128-row chunks of the tile's B
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+    static constexpr uint32_t SF_COLS_A = SF_BLK * 4;
+    static constexpr uint32_t SF_COLS = 3 * SF_BLK * 4;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t BAR_BYTES = 512;
+    static constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+    static_assert(STAGE_BYTES % 1024 == 0, "stage must keep 1024-byte alignment");
+    static_assert(256 + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    // full, sf_data, empty, sf_full per stage; accf, acc_empty; TMEM address and flags
+    static_assert((4 * STAGES + 2) * 8 + 16 <= BAR_BYTES, "barrier area");
+};
+
+__device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+template <int MAXG>
+struct PairParams {
+    CUtensorMap tma[MAXG];     // packed A, box {128 B, 128 rows}
+    CUtensorMap tmb[MAXG];     // packed B, box {128 B, 128 rows}
+    CUtensorMap tmsfa[MAXG];   // A scale blocks [blocks, 128 u32], box {128, SF_BLK}
+    CUtensorMap tmsfb[MAXG];   // B scale blocks, same
+    GemmProblemDev prob[MAXG];
+    int num_groups;
+    int total_tiles;
+};
+
+struct PairUnit {
+    int g, m_pair, n_tile;
+};
+
+// Pair tiles are numbered group by group, 256-row tiles fastest.
+template <int MAXG>
+__device__ __forceinline__ PairUnit decode_pair_unit(const PairParams<MAXG> &p, int u)
+{
+    PairUnit w;
+    int g = 0;
+#pragma unroll 1
+    while (g + 1 < p.num_groups && u >= p.prob[g + 1].tile_start) ++g;
+    w.g = g;
+    const GemmProblemDev &pr = p.prob[g];
+    const int local = u - pr.tile_start;
+    w.m_pair = local % pr.m_tiles;
+    w.n_tile = local / pr.m_tiles;
+    return w;
+}
+
+template <int KIND, int STAGES, int MAXG, bool F16>
+__global__ void __launch_bounds__(256, 1) bs_gemm_pair_kernel(const __grid_constant__ PairParams<MAXG> p)
+{
+    using Cfg = PairCfg<KIND, STAGES>;
+    constexpr bool MX = Cfg::MX;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * Cfg::STAGE_BYTES);   // rank 0: both CTAs' A/B tiles landed
+    uint64_t *sf_data = full + STAGES;      // rank 0: both CTAs' scale blocks landed
+    uint64_t *empty = sf_data + STAGES;     // the pair's MMAs are done with the stage
+    uint64_t *sf_full = empty + STAGES;     // rank 0: the stage's scales are in both TMEMs
+    uint64_t *accf = sf_full + STAGES;      // the tile's accumulator is complete
+    uint64_t *acc_empty = accf + 1;         // rank 0: both CTAs' epilogues drained it
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 1);
+    volatile int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
+    volatile int *epi_go = abort_flag + 1;  // [2] per-tile decision of the epilogue warps
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = static_cast<int>(blockIdx.x >> 1);
+    const int npairs = static_cast<int>(gridDim.x >> 1);
+    const int units = p.total_tiles;
+
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(sf_data + s, 1);
+            mbar_init(empty + s, 1);
+            mbar_init(sf_full + s, 2);   // one commit from each scale-copy thread
+        }
+        mbar_init(accf, 1);
+        mbar_init(acc_empty, 8);         // one arrival per epilogue warp of each CTA
+        *abort_flag = 0;
+        fence_mbar_init();
+        for (int g = 0; g < p.num_groups; ++g) {
+            tma_prefetch_desc(&p.tma[g]);
+            tma_prefetch_desc(&p.tmb[g]);
+            tma_prefetch_desc(&p.tmsfa[g]);
+            tma_prefetch_desc(&p.tmsfb[g]);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    // every global access waits for the preceding grid in the stream
+    grid_dependency_wait();
+    tc_fence_before();
+    cluster_sync();   // both CTAs' barriers exist before any arrival from the other CTA
+    tc_fence_after();
+    grid_launch_dependents();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem_acc = tmem;
+    const uint32_t tmem_sf = tmem + 256;
+    int issued = 0;   // stages armed by the producer (warp 0 lane 0 only)
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------------ TMA producer
+            // Rank 0 arms its barriers with both CTAs' bytes of the stage; the
+            // copies of both CTAs complete them. A rank-1 copy can land before
+            // rank 0 armed the phase (the transaction count goes negative
+            // meanwhile), never in an earlier phase: rank 1 refills a slot only
+            // after the MMAs that needed rank 0's previous phase of it.
+            // Boxes past the last row or scale block read zeros and still count
+            // their full size.
+            const uint64_t pol = policy_evict_last();
+            const uint32_t full_r0 = mapa_shared(smem_u32(full), 0);
+            const uint32_t sf_r0 = mapa_shared(smem_u32(sf_data), 0);
+            int gs = 0;
+            for (int u = pair; u < units && !*abort_flag; u += npairs) {
+                const PairUnit w = decode_pair_unit(p, u);
+                const GemmProblemDev &pr = p.prob[w.g];
+                const int a_chunk = w.m_pair * 2 + static_cast<int>(rank);   // this CTA's 128 rows of A
+                const int k_stages = (pr.k + 255) / 256;
+                for (int i = 0; i < k_stages; ++i, ++gs) {
+                    const int slot = gs % STAGES;
+                    if (gs >= STAGES &&
+                        !mbar_wait(empty + slot, ((gs / STAGES) - 1) & 1, &g_gemm_pair_error, kErrWaitEmpty)) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
+                    const int blk0 = i * Cfg::SF_BLK;
+                    if (leader) {
+                        mbar_arrive_expect_tx(sf_data + slot, 2 * (Cfg::SFA_BYTES + Cfg::SFB_BYTES));
+                        mbar_arrive_expect_tx(full + slot, 2 * (Cfg::A_BYTES + Cfg::B_BYTES));
+                    }
+                    // the scale blocks first, on their own barrier
+                    tma_load_2d_pair(st + Cfg::A_BYTES + Cfg::B_BYTES, &p.tmsfa[w.g], 0, a_chunk * pr.sf_cblocks + blk0,
+                                     sf_r0 + slot * 8, pol);
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+                        tma_load_2d_pair(st + Cfg::A_BYTES + Cfg::B_BYTES + Cfg::SFA_BYTES + j * Cfg::SF_BLK * 512,
+                                         &p.tmsfb[w.g], 0, (w.n_tile * 2 + j) * pr.sf_cblocks + blk0, sf_r0 + slot * 8,
+                                         pol);
+                    tma_load_2d_pair(st, &p.tma[w.g], i * 128, a_chunk * 128, full_r0 + slot * 8, pol);
+                    tma_load_2d_pair(st + Cfg::A_BYTES, &p.tmb[w.g], i * 128,
+                                     w.n_tile * 256 + static_cast<int>(rank) * 128, full_r0 + slot * 8, pol);
+                    issued = gs + 1;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            // --------------------------------------------- MMA issuer (rank 0)
+            constexpr uint32_t IDESC = idesc_block_scaled(256, MX, 256);
+            int gs = 0, ul = 0, commits = 0;
+            for (int u = pair; u < units; u += npairs, ++ul) {
+                const PairUnit w = decode_pair_unit(p, u);
+                const GemmProblemDev &pr = p.prob[w.g];
+                const int k_stages = (pr.k + 255) / 256;
+                const int k_steps_total = (pr.k + 63) / 64;
+                if (ul > 0 && !mbar_wait<true>(acc_empty, (ul - 1) & 1, &g_gemm_pair_error, kErrWaitAccum)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                tc_fence_after();
+                bool ok = true;
+                for (int i = 0; i < k_stages; ++i, ++gs) {
+                    const int slot = gs % STAGES;
+                    const uint32_t ph = (gs / STAGES) & 1;
+                    // one wait per stage: the scale-copy threads commit sf_full only
+                    // after they also saw the stage's operand tiles land
+                    if (!mbar_wait(sf_full + slot, ph, &g_gemm_pair_error, kErrWaitFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
+                    const uint32_t a_base = smem_u32(st);
+                    const uint32_t b_base = smem_u32(st + Cfg::A_BYTES);
+                    const uint32_t tsfa = tmem_sf + slot * Cfg::SF_COLS;
+                    const uint32_t tsfb = tsfa + Cfg::SF_COLS_A;
+                    // K step kk of the stage starts 32 bytes (2 descriptor units) further
+                    const uint64_t ad = sdesc_sw128(a_base);
+                    const uint64_t bd = sdesc_sw128(b_base);
+                    const int ksteps = min(4, k_steps_total - i * 4);
+                    auto mma_step = [&](int kk) {
+                        const int blk = MX ? kk / 2 : kk;
+                        const uint32_t sfid = MX ? static_cast<uint32_t>(kk & 1) * 2u : 0u;
+                        const uint32_t idesc = idesc_with_sf_ids(IDESC, sfid, sfid);
+                        const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                        if constexpr (MX)
+                            mma_mxf4_pair(tmem_acc, ad + 2 * kk, bd + 2 * kk, idesc, tsfa + blk * 4, tsfb + blk * 8, acc);
+                        else
+                            mma_nvf4_pair(tmem_acc, ad + 2 * kk, bd + 2 * kk, idesc, tsfa + blk * 4, tsfb + blk * 8, acc);
+                    };
+                    // the issuing thread is the bottleneck: full stages go unrolled
+                    if (ksteps == 4) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) mma_step(kk);
+                    } else {
+                        for (int kk = 0; kk < ksteps; ++kk) mma_step(kk);
+                    }
+                    tc_commit_pair_mc(empty + slot, 0x3);   // both CTAs may refill the stage
+                }
+                // arrives in both CTAs once every MMA issued above has completed
+                tc_commit_pair_mc(accf, 0x3);
+                ++commits;
+                if (!ok) {
+                    *abort_flag = 1;
+                    break;
+                }
+            }
+            // the accumulators must not be in use when the pair frees TMEM
+            if (commits > 0) mbar_wait(accf, (commits - 1) & 1, &g_gemm_pair_error, kErrWaitDrain);
+        }
+    } else if (warp == 2 || warp == 3) {
+        if (lane == 0 && leader) {
+            // ------------------------- scale staging for both CTAs (rank 0)
+            // A stage's TMEM scale slot is rewritten only after both CTAs
+            // refilled the stage's smem, which needed the MMAs' "empty" commit.
+            // Scale blocks past the problem (a second CTA without rows, a B
+            // half past N, K blocks past K) arrive as zeros and feed only
+            // accumulator rows and columns that are never stored.
+            int gs = 0;
+            for (int u = pair; u < units && !*abort_flag; u += npairs) {
+                const PairUnit w = decode_pair_unit(p, u);
+                const GemmProblemDev &pr = p.prob[w.g];
+                const int k_stages = (pr.k + 255) / 256;
+                const int k_steps_total = (pr.k + 63) / 64;
+                for (int i = 0; i < k_stages; ++i, ++gs) {
+                    const int slot = gs % STAGES;
+                    const uint32_t ph = (gs / STAGES) & 1;
+                    if (!mbar_wait(sf_data + slot, ph, &g_gemm_pair_error, kErrWaitFull)) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
+                    const uint32_t sfa_s = smem_u32(st + Cfg::A_BYTES + Cfg::B_BYTES);
+                    const uint32_t sfb_s = sfa_s + Cfg::SFA_BYTES;
+                    const uint32_t tsfa = tmem_sf + slot * Cfg::SF_COLS;
+                    const uint32_t tsfb = tsfa + Cfg::SF_COLS_A;
+                    const int ksteps = min(4, k_steps_total - i * 4);
+                    const int nblk = MX ? (ksteps + 1) / 2 : ksteps;
+                    for (int b = warp - 2; b < nblk; b += 2) {
+                        tc_cp_scale_block_pair(tsfa + b * 4, sdesc_scale(sfa_s + b * 512));
+#pragma unroll
+                        for (int j = 0; j < 2; ++j)
+                            tc_cp_scale_block_pair(tsfb + (b * 2 + j) * 4, sdesc_scale(sfb_s + (j * Cfg::SF_BLK + b) * 512));
+                    }
+                    // the MMA issuer waits only for sf_full: it also stands for the
+                    // stage's operand tiles
+                    if (!mbar_wait(full + slot, ph, &g_gemm_pair_error, kErrWaitFull)) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    tc_commit_pair(sf_full + slot);
+                }
+            }
+            // copies still in flight (only after an abort) finish before TMEM is freed
+            for (int i = max(0, gs - STAGES); i < gs; ++i)
+                mbar_wait(sf_full + (i % STAGES), (i / STAGES) & 1, &g_gemm_pair_error, kErrWaitDrain);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;                  // TMEM lane quadrant of this warp
+        const int row_in_tile = q * 32 + lane;
+        const uint32_t t_row = tmem_acc + (static_cast<uint32_t>(q * 32) << 16);
+        const uint32_t acc_empty_r0 = mapa_shared(smem_u32(acc_empty), 0);
+        int ul = 0;
+        for (int u = pair; u < units; u += npairs, ++ul) {
+            const PairUnit w = decode_pair_unit(p, u);
+            const GemmProblemDev &pr = p.prob[w.g];
+            // one thread waits and decides for the four warps, so that they
+            // leave the loop together
+            if (threadIdx.x == 128) {
+                const bool ok = mbar_wait(accf, ul & 1, &g_gemm_pair_error, kErrWaitAccum);
+                if (!ok) *abort_flag = 1;
+                epi_go[ul & 1] = ok;
+            }
+            epilogue_bar();
+            if (!epi_go[ul & 1]) break;
+            tc_fence_after();
+            const bool run = (*abort_flag == 0);
+            const int row = w.m_pair * 256 + static_cast<int>(rank) * 128 + row_in_tile;
+            // drain the row into registers, hand TMEM back, then store
+            uint32_t pk[128];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint32_t v[32];
+                tmem_ld32(t_row + c * 32, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    pk[c * 16 + j] = pack2<F16>(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acc_empty_r0);
+            if (run && row < pr.m) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const int col0 = w.n_tile * 256 + c * 32;
+                    if (col0 < pr.n) {
+                        uint32_t part[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) part[j] = pk[c * 16 + j];
+                        store_packed32(pr.c, pr.ldc, row, col0, pr.n, part);
+                    }
+                }
+            }
+        }
+    }
+    __syncwarp();
+
+    // ----------------------------------------------------------- teardown
+    tc_fence_before();
+    if (warp == 0 && lane == 0 && leader) {
+        // copies still in flight (only after an abort) must land before exit;
+        // rank 0's barriers count both CTAs' copies
+        for (int i = max(0, issued - STAGES); i < issued; ++i) {
+            mbar_wait(sf_data + (i % STAGES), (i / STAGES) & 1, &g_gemm_pair_error, kErrWaitDrain);
+            mbar_wait(full + (i % STAGES), (i / STAGES) & 1, &g_gemm_pair_error, kErrWaitDrain);
+        }
+    }
+    // neither CTA leaves while the other may still arrive on its barriers or
+    // use its shared memory and TMEM
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, Cfg::TMEM_COLS);
+    }
+}
+
+template <int KIND, int STAGES, int MAXG, bool F16>
+cudaError_t launch_pair(const PairParams<MAXG> &params, cudaStream_t stream)
+{
+    using Cfg = PairCfg<KIND, STAGES>;
+    auto kern = bs_gemm_pair_kernel<KIND, STAGES, MAXG, F16>;
+    static uint64_t configured = 0;  // one bit per device; setting it twice is harmless
+    static int sms_of[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (!(configured & (1ull << (dev & 63)))) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&sms_of[dev & 63], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        configured |= 1ull << (dev & 63);
+    }
+    const int pairs = min(params.total_tiles, max(1, sms_of[dev & 63] / 2));
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(2 * pairs, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kern, params);
+}
+
+constexpr int kPairMxStages = 6;   // 35 KB stages
+constexpr int kPairNvStages = 5;   // 38 KB stages; TMEM holds 5 stages of NVFP4 scales
+
+// Pair tiles: 256 rows of A (two CTAs) x 256 columns.
+template <int MAXG>
+void fill_pair_problem(PairParams<MAXG> &P, int g, const GemmProblemHost &h, int vec, int &tiles)
+{
+    P.tma[g] = h.tma;
+    P.tmb[g] = h.tmb;
+    P.tmsfa[g] = h.tmsfa;
+    P.tmsfb[g] = h.tmsfb;
+    GemmProblemDev &d = P.prob[g];
+    d.sfa = h.sfa;
+    d.sfb = h.sfb;
+    d.c = h.c;
+    d.ldc = h.ldc;
+    d.m = h.m;
+    d.n = h.n;
+    d.k = h.k;
+    d.m_tiles = (h.m + 255) / 256;
+    d.n_tiles = (h.n + 255) / 256;
+    d.tile_start = tiles;
+    d.sf_cblocks = (h.k / vec + 3) / 4;
+    d.pad_ = 0;
+    tiles += d.m_tiles * d.n_tiles;
+}
+
+}  // namespace
+
+int pair_tiles(int64_t m, int64_t n) { return static_cast<int>(((m + 255) / 256) * ((n + 255) / 256)); }
+
+cudaError_t launch_gemm_mx_pair(const GemmProblemHost &prob, cudaStream_t stream)
+{
+    PairParams<1> P;
+    memset(&P, 0, sizeof(P));
+    int tiles = 0;
+    fill_pair_problem(P, 0, prob, 32, tiles);
+    P.num_groups = 1;
+    P.total_tiles = tiles;
+    return launch_pair<0, kPairMxStages, 1, false>(P, stream);
+}
+
+cudaError_t launch_gemm_nv_grouped_pair(const GemmProblemHost *probs, int num_groups, cudaStream_t stream)
+{
+    PairParams<kMaxGroups> P;
+    memset(&P, 0, sizeof(P));
+    int tiles = 0;
+    for (int g = 0; g < num_groups; ++g) fill_pair_problem(P, g, probs[g], 16, tiles);
+    P.num_groups = num_groups;
+    P.total_tiles = tiles;
+    return launch_pair<1, kPairNvStages, kMaxGroups, true>(P, stream);
+}
+
+int read_and_clear_gemm_pair_error()
+{
+    int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_gemm_pair_error, sizeof(int)) != cudaSuccess) return -1;
+    cudaMemcpyToSymbol(g_gemm_pair_error, &zero, sizeof(int));
+    return v;
+}
+
+}  // namespace mxfp4

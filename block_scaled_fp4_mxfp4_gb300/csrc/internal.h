@@ -26,6 +26,10 @@ struct GemmProblemHost {
     void *c;                  // bf16 (MXFP4) or fp16 (NVFP4) [m, n]
     int64_t ldc;              // elements
     int m, n, k;
+    // CTA-pair kernels only: the scale buffers as [blocks, 128 u32] with a box of
+    // one stage's K-blocks (2 for MXFP4, 4 for NVFP4)
+    CUtensorMap tmsfa;
+    CUtensorMap tmsfb;
 };
 
 // Tile width along N of the grouped NVFP4 GEMM (box rows of tmb).
@@ -40,6 +44,16 @@ cudaError_t launch_gemm_mx(const GemmProblemHost &prob, int bn, int splits, floa
 cudaError_t launch_gemm_nv_grouped(const GemmProblemHost *probs, int num_groups,
                                    cudaStream_t stream);
 int read_and_clear_gemm_error();
+
+// ------------------------------------------------------------ gemm_pair.cu
+// The same GEMMs on CTA pairs (tcgen05 cta_group::2, 256 x 256 tiles, no
+// split-K) for problems with enough tiles to fill the GPU. prob.tmb boxes are
+// 128 rows (each CTA loads half of a tile's B).
+int pair_tiles(int64_t m, int64_t n);   // 256 x 256 tiles of an m x n output
+cudaError_t launch_gemm_mx_pair(const GemmProblemHost &prob, cudaStream_t stream);
+cudaError_t launch_gemm_nv_grouped_pair(const GemmProblemHost *probs, int num_groups,
+                                        cudaStream_t stream);
+int read_and_clear_gemm_pair_error();
 
 // ---------------------------------------------------------------- fused.cu
 struct FusedPlan {

@@ -17,6 +17,7 @@ enum DeviceError : int {
     kErrWaitAccum = 3,    // epilogue waited too long for the accumulator
     kErrWaitOperand = 4,  // MMA issuer waited too long for on-chip quantized A
     kErrWaitDrain = 5,    // exit path waited too long for copies in flight
+    kErrWaitPeer = 6,     // waited too long for the other CTA of a pair
 };
 
 // A wait gives up after this many nanoseconds of %globaltimer.
@@ -60,32 +61,52 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// CLUSTER: acquire at cluster scope, for phases completed by arrivals from
+// another CTA of the cluster (arriving with release at cluster scope).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
+    if constexpr (CLUSTER)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
     return ok != 0;
 }
 
 // Waits for the phase with the given parity to complete. Returns false after
 // kWaitTimeoutNs, having recorded `code` in *err (first error wins).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err, int code)
 {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
         if (global_timer_ns() - t0 > kWaitTimeoutNs) {
             atomicCAS(err, 0, code);
             return false;
         }
     }
+}
+
+// Arrive on an mbarrier of a CTA of this cluster (address from mapa_shared);
+// the release orders this thread's earlier memory accesses before it.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // --------------------------------------------------------------------- TMA
@@ -214,6 +235,94 @@ __device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
+// ------------------------------------------- CTA pairs (tcgen05 cta_group::2)
+// A kernel uses one cta_group for all of its tcgen05 instructions. With
+// cta_group::2 the two CTAs of a cluster pair (ranks 0 and 1) allocate and
+// free the same TMEM columns together (one warp of each CTA executes the
+// alloc / relinquish / dealloc), and one thread of rank 0 issues the MMAs and
+// scale copies for both: each CTA supplies its operands and scale blocks from
+// its own shared memory at the same offsets, and each CTA's TMEM holds the
+// accumulator rows and scales of its own 128 rows.
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *smem_result, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(smem_result)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Arrives on `bar` of this CTA once this thread's earlier pair MMAs / copies
+// have completed.
+__device__ __forceinline__ void tc_commit_pair(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Same, arriving on the barrier at `bar`'s offset in every CTA of `cta_mask`.
+__device__ __forceinline__ void tc_commit_pair_mc(uint64_t *bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
+// Copies each CTA's 512-byte scale block at `sdesc` into its own TMEM.
+__device__ __forceinline__ void tc_cp_scale_block_pair(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// D (+)= A x B^T over the pair: M = 256 (128 rows from each CTA), N from the
+// instruction descriptor (N/2 rows of B from each CTA).
+__device__ __forceinline__ void mma_mxf4_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_nvf4_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// 2-D tiled load into this CTA's shared memory that completes the transaction
+// count of `bar_cluster`, an mbarrier of either CTA of the pair (shared::cluster
+// address from mapa_shared): the pair's operand loads all complete rank 0's
+// barriers.
+__device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const CUtensorMap *tm, int32_t x, int32_t y,
+                                                 uint32_t bar_cluster, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar_cluster), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
 // Loads 32 consecutive fp32 columns of this warp's 32 TMEM lanes.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
 {
@@ -271,16 +380,16 @@ __device__ __forceinline__ uint64_t sdesc_scale(uint32_t saddr)
 }
 
 // Instruction descriptor of a block-scaled MMA with E2M1 operands, K-major A
-// and B, M = 128 and the given N. `ue8m0` selects E8M0 scales (else E4M3).
+// and B, the given N and M (128, or 256 for a CTA-pair MMA). `ue8m0` selects E8M0 scales (else E4M3).
 // The scale-factor IDs (which bytes of the 32-bit TMEM scale cell an MMA
 // uses) go in bits 29-30 (A) and 4-5 (B).
-__host__ __device__ constexpr uint32_t idesc_block_scaled(int n, bool ue8m0)
+__host__ __device__ constexpr uint32_t idesc_block_scaled(int n, bool ue8m0, int m = 128)
 {
     return (1u << 7)                                    // A format E2M1
            | (1u << 10)                                 // B format E2M1
            | (static_cast<uint32_t>(n >> 3) << 17)      // N / 8
            | ((ue8m0 ? 1u : 0u) << 23)                  // scale type
-           | (static_cast<uint32_t>(128 >> 4) << 24);   // M / 16
+           | (static_cast<uint32_t>(m >> 4) << 24);     // M / 16
 }
 
 __device__ __forceinline__ uint32_t idesc_with_sf_ids(uint32_t idesc, uint32_t a_id, uint32_t b_id)

@@ -53,6 +53,11 @@ def test_eight_groups_small_k():
     run_groups(shapes, 3)
 
 
+def test_groups_on_cta_pairs_ragged():
+    # 110 tiles of 256 x 256 in total: the CTA-pair kernel; ragged M, N and K
+    run_groups([(100, 2600, 272), (700, 2600, 512), (1300, 2600, 96)], 3)
+
+
 def test_sixteen_groups_max():
     shapes = [(16 + 8 * i, 128 + 64 * (i % 3), 128 + 32 * (i % 4)) for i in range(16)]
     run_groups(shapes, 4)
