@@ -78,6 +78,24 @@ def kernel_source_hash(files):
     return h.hexdigest()[:16]
 
 
+KERNEL_SOURCES = {
+    "fused_quant_gemm_kernel": ["fused.cu", "ptx.cuh", "quant_math.cuh"],
+    "bs_gemm_kernel": ["gemm.cu", "gemm_common.cuh", "ptx.cuh"],
+    "bs_gemm_pair_kernel": ["gemm_pair.cu", "gemm_common.cuh", "ptx.cuh"],
+}
+
+
+def kernel_of(plan, kind):
+    """(label, source files) of the GEMM kernel a call's plan launches."""
+    name = plan["kernel"]
+    if name == "fused_quant_gemm_kernel":
+        label = f"{name}<{plan['tile_m']}> x{plan['tiles']} tiles, {plan['splits']}-CTA K-split clusters"
+    else:
+        label = (f"{name}<{kind}> {plan['tile_m']}x{plan['tile_n']} tiles x{plan['tiles']}"
+                 + (f", {plan['splits']} K-splits" if plan["splits"] > 1 else ""))
+    return label, KERNEL_SOURCES[name]
+
+
 def ncu_traffic(workload, kernel_files):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary table, or None if that kernel's source changed since the capture."""
@@ -172,7 +190,8 @@ class MXCase:
         self.ws = mx.new_workspace(w.M, w.N, w.K, dev)
         self.fused = w.M <= 64      # the library's fused small-M path (one launch)
         self.launches_per_step = 1 if self.fused else 2
-        self.kernel_files = ["fused.cu", "ptx.cuh", "quant_math.cuh"] if self.fused else ["gemm.cu", "ptx.cuh"]
+        plan = mx.gemm_plan(w.M, w.N, w.K, fused=True)
+        self.kernel_label, self.kernel_files = kernel_of(plan, "mxf4")
         self.rot_bytes = per * self.rot
 
     def step(self, i):
@@ -238,7 +257,7 @@ class NVCase:
         self.problems = mx.make_nv_problems(self.groups)
         self.rot = 1                # 178 MB of operands per call already exceed twice the L2
         self.launches_per_step = 1
-        self.kernel_files = ["gemm.cu", "ptx.cuh"]
+        self.kernel_label, self.kernel_files = kernel_of(mx.nvfp4_group_gemm_plan(self.problems), "mxf4nvf4")
         self.rot_bytes = w.alg_bytes
 
     def step(self, i):
@@ -363,19 +382,13 @@ def run_ours(args, name, rank, world, local_rank):
         roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
                 "frac": round(ach / fp4_peak, 4),
                 "peak_source": f"{peak_src} bf16 sustained x {FP4_OVER_BF16:g} (nominal FP4:BF16)"}
-        kname = "bs_gemm_kernel<mxf4>"
     else:
-        if name == "medium":
-            nbytes = case.gemm_alg_bytes()
-            kname = "bs_gemm_kernel<mxf4>"
-        else:
-            nbytes = case.alg_bytes()
-            kname = "fused_quant_gemm_kernel" if name != "nvfp4_grouped" else "bs_gemm_kernel<mxf4nvf4>"
+        nbytes = case.gemm_alg_bytes() if name == "medium" else case.alg_bytes()
         ach = nbytes / (per_kernel_us * 1e-6) / 1e9
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(ach / peaks["hbm_gbs"], 4), "peak_source": f"{peak_src} hbm_gbs"}
     roof["traffic"] = ncu_traffic(name, case.kernel_files)
-    roof["kernel"] = kname
+    roof["kernel"] = case.kernel_label
     roof["kernel_us"] = round(per_kernel_us, 3)
     roof["kernel_timing"] = kernel_timing
 

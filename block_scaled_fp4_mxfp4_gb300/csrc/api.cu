@@ -448,6 +448,63 @@ mxfp4_status_t nvfp4_group_gemm(const nvfp4_problem_t *problems, int num_groups,
     return cuda_status(launch_gemm_nv_grouped(hp, num_groups, static_cast<cudaStream_t>(stream)));
 }
 
+mxfp4_status_t mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, int which, mxfp4_plan_t *out)
+{
+    if (!out || (which != 0 && which != 1)) return MXFP4_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return MXFP4_ERR_INVALID_ARG;
+    if (K % 32 != 0) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+    int sms = 0;
+    const mxfp4_status_t st = current_device(&sms);
+    if (st != MXFP4_OK) return st;
+    memset(out, 0, sizeof(*out));
+    FusedPlan fp;
+    if (which == 1 && plan_fused(M, N, K, sms, &fp)) {
+        out->kernel = MXFP4_KERNEL_FUSED;
+        out->tile_m = fp.mma_n;   // activation rows (padded) x 128 weight rows
+        out->tile_n = 128;
+        out->splits = fp.splits;
+        out->tiles = fp.n_tiles;
+        out->quant_launch = 0;
+        return MXFP4_OK;
+    }
+    const GemmPlan gp = plan_gemm(M, N, K);
+    out->kernel = gp.pair ? MXFP4_KERNEL_GEMM_PAIR : MXFP4_KERNEL_GEMM;
+    out->tile_m = gp.pair ? 256 : 128;
+    out->tile_n = gp.pair ? 256 : gp.bn;
+    out->splits = gp.splits;
+    out->tiles = gp.tiles;
+    out->quant_launch = which;
+    return MXFP4_OK;
+}
+
+mxfp4_status_t nvfp4_group_gemm_plan(const nvfp4_problem_t *problems, int num_groups, mxfp4_plan_t *out)
+{
+    if (!out || !problems || num_groups < 1) return MXFP4_ERR_INVALID_ARG;
+    if (num_groups > NVFP4_MAX_GROUPS) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+    int64_t tiles = 0, pair_tile_count = 0;
+    const int bn = gemm_block_n_nv();
+    for (int g = 0; g < num_groups; ++g) {
+        const nvfp4_problem_t &p = problems[g];
+        if (p.m < 1 || p.n < 1 || p.k < 1 || p.m > kMaxDim || p.n > kMaxDim || p.k > kMaxDim)
+            return MXFP4_ERR_INVALID_ARG;
+        if (p.k % 16 != 0) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+        tiles += ((p.m + 127) / 128) * ((p.n + bn - 1) / bn);
+        pair_tile_count += pair_tiles(p.m, p.n);
+    }
+    int sms = 0;
+    const mxfp4_status_t st = current_device(&sms);
+    if (st != MXFP4_OK) return st;
+    memset(out, 0, sizeof(*out));
+    const bool pair = use_pair(pair_tile_count);
+    out->kernel = pair ? MXFP4_KERNEL_GEMM_PAIR : MXFP4_KERNEL_GEMM;
+    out->tile_m = pair ? 256 : 128;
+    out->tile_n = pair ? 256 : bn;
+    out->splits = 1;
+    out->tiles = static_cast<int>(pair ? pair_tile_count : tiles);
+    out->quant_launch = 0;
+    return MXFP4_OK;
+}
+
 mxfp4_status_t mxfp4_get_device_error(int *code)
 {
     if (!code) return MXFP4_ERR_INVALID_ARG;

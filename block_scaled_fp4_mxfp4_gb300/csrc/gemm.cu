@@ -186,8 +186,9 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
                 for (int i = 0; i < w.nst; ++i, ++gs) {
                     const int slot = gs % STAGES;
                     const uint32_t ph = (gs / STAGES) & 1;
-                    if (!mbar_wait(full + slot, ph, &g_gemm_error, kErrWaitFull) ||
-                        !mbar_wait(sf_full + slot, ph, &g_gemm_error, kErrWaitFull)) {
+                    // one wait per stage: the scale-copy threads commit sf_full only
+                    // after they also saw the stage's operand tiles land
+                    if (!mbar_wait(sf_full + slot, ph, &g_gemm_error, kErrWaitFull)) {
                         ok = false;
                         break;
                     }
@@ -198,18 +199,26 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
                     const uint32_t tsfa = tmem_sf + slot * Cfg::SF_COLS;
                     const uint32_t tsfb = tsfa + Cfg::SF_COLS_A;
                     const int ks = w.s_begin + i;
+                    // K step kk of the stage starts 32 bytes (2 descriptor units) further
+                    const uint64_t ad = sdesc_sw128(a_base);
+                    const uint64_t bd = sdesc_sw128(b_base);
                     const int ksteps = min(4, k_steps_total - ks * 4);
-                    for (int kk = 0; kk < ksteps; ++kk) {
-                        const uint64_t ad = sdesc_sw128(a_base + kk * 32);
-                        const uint64_t bd = sdesc_sw128(b_base + kk * 32);
+                    auto mma_step = [&](int kk) {
                         const int blk = MX ? kk / 2 : kk;
                         const uint32_t sfid = MX ? static_cast<uint32_t>(kk & 1) * 2u : 0u;
                         const uint32_t idesc = idesc_with_sf_ids(IDESC, sfid, sfid);
                         const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
                         if constexpr (MX)
-                            mma_mxf4(tmem_acc, ad, bd, idesc, tsfa + blk * 4, tsfb + blk * Cfg::NCH * 4, acc);
+                            mma_mxf4(tmem_acc, ad + 2 * kk, bd + 2 * kk, idesc, tsfa + blk * 4, tsfb + blk * Cfg::NCH * 4, acc);
                         else
-                            mma_nvf4(tmem_acc, ad, bd, idesc, tsfa + blk * 4, tsfb + blk * Cfg::NCH * 4, acc);
+                            mma_nvf4(tmem_acc, ad + 2 * kk, bd + 2 * kk, idesc, tsfa + blk * 4, tsfb + blk * Cfg::NCH * 4, acc);
+                    };
+                    // the issuing thread is the bottleneck: full stages go unrolled
+                    if (ksteps == 4) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) mma_step(kk);
+                    } else {
+                        for (int kk = 0; kk < ksteps; ++kk) mma_step(kk);
                     }
                     tc_commit(empty + slot);
                 }
@@ -261,6 +270,12 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
                         for (int j = 0; j < Cfg::NCH; ++j)
                             tc_cp_scale_block(tsfb + (b * Cfg::NCH + j) * 4,
                                               sdesc_scale(sfb_s + (j * Cfg::SF_BLK + b) * 512));
+                    }
+                    // the MMA issuer waits only for sf_full: it also stands for the
+                    // stage's operand tiles
+                    if (!mbar_wait(full + slot, (gs / STAGES) & 1, &g_gemm_error, kErrWaitFull)) {
+                        *abort_flag = 1;
+                        break;
                     }
                     tc_commit(sf_full + slot);
                 }

@@ -42,6 +42,15 @@ class NvProblem(ctypes.Structure):
                 ("lda", _i64), ("ldb", _i64), ("ldc", _i64)]
 
 
+class Plan(ctypes.Structure):
+    """mxfp4_plan_t: the kernel and tiling a call launches."""
+    _fields_ = [("kernel", ctypes.c_int), ("tile_m", ctypes.c_int), ("tile_n", ctypes.c_int),
+                ("splits", ctypes.c_int), ("tiles", ctypes.c_int), ("quant_launch", ctypes.c_int)]
+
+
+KERNEL_NAMES = {1: "fused_quant_gemm_kernel", 2: "bs_gemm_kernel", 3: "bs_gemm_pair_kernel"}
+
+
 def _load(path: str = LIB_PATH) -> ctypes.CDLL:
     if not os.path.exists(path):
         raise ImportError(
@@ -74,6 +83,10 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.mxfp4_gemm_a4w4_noalloc.argtypes = [_p, _i64, _p, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p]
     L.mxfp4_get_device_error.restype = _st
     L.mxfp4_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    L.mxfp4_gemm_plan.restype = _st
+    L.mxfp4_gemm_plan.argtypes = [_i64, _i64, _i64, ctypes.c_int, ctypes.POINTER(Plan)]
+    L.nvfp4_group_gemm_plan.restype = _st
+    L.nvfp4_group_gemm_plan.argtypes = [ctypes.POINTER(NvProblem), ctypes.c_int, ctypes.POINTER(Plan)]
     return L
 
 
@@ -228,6 +241,26 @@ def nvfp4_group_gemm(groups, problems=None, stream=None):
     _check(_lib.nvfp4_group_gemm(problems, len(problems), None, 0, _stream_ptr(stream)),
            "nvfp4_group_gemm")
     return [g["c"] for g in groups]
+
+
+def _plan_dict(p: Plan) -> dict:
+    return dict(kernel=KERNEL_NAMES.get(p.kernel, str(p.kernel)), tile_m=p.tile_m, tile_n=p.tile_n,
+                splits=p.splits, tiles=p.tiles, quant_launch=bool(p.quant_launch))
+
+
+def gemm_plan(M: int, N: int, K: int, fused: bool = False) -> dict:
+    """What mxfp4_gemm_a4w4 (fused=False) or mxfp4_quant_gemm_fused (fused=True)
+    launches for an M x N x K problem on the current device."""
+    p = Plan()
+    _check(lib().mxfp4_gemm_plan(M, N, K, 1 if fused else 0, ctypes.byref(p)), "mxfp4_gemm_plan")
+    return _plan_dict(p)
+
+
+def nvfp4_group_gemm_plan(problems) -> dict:
+    """What nvfp4_group_gemm launches for these problems (see make_nv_problems)."""
+    p = Plan()
+    _check(lib().nvfp4_group_gemm_plan(problems, len(problems), ctypes.byref(p)), "nvfp4_group_gemm_plan")
+    return _plan_dict(p)
 
 
 def get_device_error() -> int:

@@ -218,6 +218,32 @@ MXFP4_API mxfp4_status_t mxfp4_gemm_a4w4_noalloc(const void *Aq, int64_t ldaq, c
 
 /* ------------------------------------------------------------ diagnostics -- */
 
+/* Kernels a call can launch (mxfp4_plan_t.kernel). */
+#define MXFP4_KERNEL_FUSED 1      /* fused quantization + GEMM, swap-AB, K-split clusters */
+#define MXFP4_KERNEL_GEMM 2       /* single-CTA block-scaled GEMM, 128 x tile_n tiles */
+#define MXFP4_KERNEL_GEMM_PAIR 3  /* CTA-pair GEMM (tcgen05 cta_group::2), 256 x 256 tiles */
+
+/* What a call launches: the GEMM kernel, the output tile one CTA (pair:
+ * one CTA pair) computes, the K-splits per tile, the number of output tiles,
+ * and whether a separate quantization kernel runs first. */
+typedef struct {
+    int kernel;
+    int tile_m, tile_n;
+    int splits;
+    int tiles;
+    int quant_launch;
+} mxfp4_plan_t;
+
+/* The plan of mxfp4_gemm_a4w4 (which = 0) or mxfp4_quant_gemm_fused
+ * (which = 1) for an M x N x K problem on the current device. Launches
+ * nothing; reads the device's SM count (MXFP4_ERR_NO_DEVICE without a usable
+ * GB300). Argument checks as for the calls themselves, minus the pointers. */
+MXFP4_API mxfp4_status_t mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, int which, mxfp4_plan_t *out);
+
+/* The plan of nvfp4_group_gemm for these problems (pointers are not read). */
+MXFP4_API mxfp4_status_t nvfp4_group_gemm_plan(const nvfp4_problem_t *problems, int num_groups,
+                                               mxfp4_plan_t *out);
+
 /* Reads and clears the library's device-side error word. Kernels never trap:
  * a wait that exceeds its time limit (about 2 s) records a nonzero code there
  * and the kernel exits cleanly. This call synchronizes the current device.

@@ -14,7 +14,7 @@ L = mxfp4.lib()
 
 def test_every_declared_symbol_is_exported():
     names = mxfp4.declared_symbols()
-    assert len(names) == 13
+    assert len(names) == 15
     for n in names:
         assert hasattr(L, n), n  # ctypes resolves the exported symbol
 
@@ -100,3 +100,21 @@ def test_valid_call_without_gpu_reports_no_device():
     assert L.mxfp4_quantize(16, 1, 32, 32, 16, 16, 16, None) == 7
     code = ctypes.c_int(-1)
     assert L.mxfp4_get_device_error(ctypes.byref(code)) == 5
+
+
+def test_plan_argument_validation_needs_no_gpu():
+    plan = mxfp4.Plan()
+    assert L.mxfp4_gemm_plan(16, 2112, 7168, 1, None) == 1          # no output struct
+    assert L.mxfp4_gemm_plan(16, 2112, 7168, 2, ctypes.byref(plan)) == 1   # which must be 0 or 1
+    assert L.mxfp4_gemm_plan(0, 2112, 7168, 0, ctypes.byref(plan)) == 1
+    assert L.mxfp4_gemm_plan(16, 2112, 7000, 0, ctypes.byref(plan)) == 2   # K % 32
+    probs = (mxfp4.NvProblem * 1)()
+    probs[0] = mxfp4.NvProblem(64, 256, 100, 16, 16, 16, 16, 16, 64, 128, 256)
+    assert L.nvfp4_group_gemm_plan(probs, 1, ctypes.byref(plan)) == 2      # K % 16
+    assert L.nvfp4_group_gemm_plan(probs, 17, ctypes.byref(plan)) == 2     # too many groups
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="checks the no-GPU answer")
+def test_plan_without_gpu_reports_no_device():
+    plan = mxfp4.Plan()
+    assert L.mxfp4_gemm_plan(16, 2112, 7168, 1, ctypes.byref(plan)) == 7

@@ -84,3 +84,25 @@ def test_nvfp4_grouped_sampled():
         got = gd["c"][torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].float().cpu().numpy()
         assert_within_tolerance(got.astype(np.float64), c_ref, s, f"nvfp4 group {g} (sampled)")
     assert mx.get_device_error() == 0
+
+
+def test_plans_of_the_benchmarked_calls():
+    """The kernel each benchmarked call launches (what bench.py reports)."""
+    p = mx.gemm_plan(wl.DECODE.M, wl.DECODE.N, wl.DECODE.K, fused=True)
+    assert p["kernel"] == "fused_quant_gemm_kernel" and p["tile_m"] == 16 and p["tiles"] == 17
+    assert 1 <= p["splits"] <= 8 and not p["quant_launch"]
+    p = mx.gemm_plan(wl.MEDIUM.M, wl.MEDIUM.N, wl.MEDIUM.K, fused=True)
+    assert p["kernel"] == "bs_gemm_kernel" and (p["tile_m"], p["tile_n"]) == (128, 128) and p["quant_launch"]
+    p = mx.gemm_plan(wl.COMPUTE.M, wl.COMPUTE.N, wl.COMPUTE.K)
+    assert p["kernel"] == "bs_gemm_pair_kernel" and p["tiles"] == 32 * 32 and p["splits"] == 1
+    w = wl.NVFP4_GROUPED
+    groups = []
+    for m in w.Ms:
+        groups.append(dict(a=torch.zeros((m, w.K // 2), dtype=torch.uint8, device="cuda"),
+                           sfa=torch.zeros(mx.sf_bytes(m, w.K, 16), dtype=torch.uint8, device="cuda"),
+                           b=torch.zeros((w.N, w.K // 2), dtype=torch.uint8, device="cuda"),
+                           sfb=torch.zeros(mx.sf_bytes(w.N, w.K, 16), dtype=torch.uint8, device="cuda"),
+                           c=torch.zeros((m, w.N), dtype=torch.float16, device="cuda"), k=w.K))
+    p = mx.nvfp4_group_gemm_plan(mx.make_nv_problems(groups))
+    assert p["kernel"] == "bs_gemm_pair_kernel"
+    assert p["tiles"] == sum((m + 255) // 256 for m in w.Ms) * (w.N // 256)
