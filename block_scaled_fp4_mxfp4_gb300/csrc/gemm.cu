@@ -9,16 +9,22 @@
 // its custom_kernel loop over problems, here replaced by one launch whose
 // blocks map a linear tile id to (problem, m-tile, n-tile) by prefix sums.
 //
-// One CTA computes one 128 x BN output tile (optionally one K-split of it):
+// Single-CTA kernel, for problems too small to give every SM pair a 256 x 256
+// tile (larger ones go to the CTA-pair kernel in gemm_pair.cu). Persistent:
+// one CTA per SM walks the 128 x BN output tiles (BN = 256, or 128 when
+// 256-wide tiles would leave most SMs idle), optionally split along K:
 //   warp 0 lane 0  TMA producer: A/B 128-byte-swizzled K-major tiles (256 FP4
-//                  per row = 128 bytes per stage) and the stage's 512-byte
-//                  scale blocks (1-D bulk copies straight from the blocked
-//                  layout: consecutive K-blocks of 128 rows are contiguous).
-//   warp 1         allocates TMEM; lane 0 issues tcgen05.cp (scales smem ->
-//                  TMEM, one TMEM slot per pipeline stage) and four MMAs of
-//                  K = 64 per stage, then commits the stage's "empty" barrier.
-//   warps 0-3      epilogue: tcgen05.ld of the fp32 accumulator (warp w owns
-//                  TMEM lanes 32w..32w+31 = output rows), convert, store.
+//                  per row = 128 bytes per stage) and, first and on their own
+//                  barrier, the stage's 512-byte scale blocks (1-D bulk copies
+//                  straight from the blocked layout: consecutive K-blocks of
+//                  128 rows are contiguous).
+//   warp 1         allocates TMEM; lane 0 issues the four K = 64 MMAs of each
+//                  stage and commits the stage's "empty" barrier.
+//   warps 2, 3     lane 0 of each copies half of every stage's scale blocks
+//                  smem -> TMEM (one TMEM slot per pipeline stage).
+//   warps 4-7      epilogue: tcgen05.ld of the fp32 accumulator (TMEM lane
+//                  quadrant = warp % 4 = output rows), convert, store, while
+//                  the next tile's mainloop runs.
 // Split-K (splits > 1): each split writes fp32 partials to the workspace; the
 // last split to arrive (atomic ticket) sums them in split order and writes C,
 // then resets its ticket so the workspace stays zeroed.
