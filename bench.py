@@ -49,6 +49,23 @@ WORKLOADS = {
 DEFAULT_STEPS = {"decode": 20000, "tiny": 20000, "medium": 10000, "compute": 50, "nvfp4_grouped": 500}
 
 
+def max_over_ranks(value, world, device):
+    """The largest of every rank's value: a job's time is its slowest rank's."""
+    if world == 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_us_per_call(elapsed_ms, steps, world):
+    """Whole-job microseconds per call: `world` replicas each made `steps` calls
+    within elapsed_ms (the slowest rank's time)."""
+    return elapsed_ms * 1000.0 / (steps * world)
+
+
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -417,13 +434,8 @@ def run_ours(args, name, rank, world, local_rank):
         split_times = {"gemm_us": per_kernel_us, "step_us": elapsed_ms * 1000.0 / steps}
         kernel_timing = "GEMM kernel timed alone: CUDA-graph replay of --steps launches"
 
-    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        import torch.distributed as dist
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    elapsed_ms = float(t.item())
-
-    us_per_call = elapsed_ms * 1000.0 / (steps * world)
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
+    us_per_call = job_us_per_call(elapsed_ms, steps, world)
     tflops = w.flops * steps * world / (elapsed_ms * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
     clocks = clk.summary()
@@ -466,11 +478,8 @@ def run_ours(args, name, rank, world, local_rank):
         short = case.launches_per_step == 1 and name != "nvfp4_grouped"
         e2e_steps = max(10, min(steps, 2000 if short else 20))
         e_us, h2d, d2h = case.e2e(e2e_steps, torch)
-        t = torch.tensor([e_us], dtype=torch.float64, device=dev)
-        if world > 1:
-            import torch.distributed as dist
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        line["e2e"] = {"value": round(float(t.item()) / world, 4), "unit": "us/call",
+        e_us = max_over_ranks(e_us, world, dev) / world
+        line["e2e"] = {"value": round(e_us, 4), "unit": "us/call",
                        "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -1,0 +1,63 @@
+"""bench.py's multi-rank bookkeeping on CPU: world_size-2 gloo ranks agree on
+the slowest rank's time and on the whole-job time per call; a non-zero rank of
+the reference arm exits without work. No GPU."""
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, out):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    sys.path.insert(0, ROOT)
+    import bench
+    slowest = bench.max_over_ranks(10.0 + 3.0 * rank, world, "cpu")   # rank 1 is slower
+    out.put((rank, slowest, bench.job_us_per_call(slowest, 100, world)))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_ranks_take_the_slowest_time_and_aggregate_calls():
+    ctx = mp.get_context("spawn")
+    out = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(out.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [g[1] for g in got] == [13.0, 13.0]
+    # 2 ranks x 100 calls in 13 ms -> 65 us per call for the whole job
+    assert all(abs(g[2] - 65.0) < 1e-9 for g in got)
+
+
+def test_single_rank_needs_no_process_group():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(4.5, 1, "cpu") == 4.5
+    assert bench.job_us_per_call(4.5, 10, 1) == 450.0
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference"],
+                       env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
