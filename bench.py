@@ -5,6 +5,7 @@ A step is one call of the hot path on one batch of synthetic input:
   decode (default)  mxfp4_quant_gemm_fused, A bf16 [16, 7168] x MXFP4 B [2112, 7168]
   tiny / medium / compute   the other MXFP4 quant+GEMM shapes
   nvfp4_grouped     nvfp4_group_gemm over 8 groups (M_g 64..1024, N 4096, K 7168)
+  mxfp4_grouped     mxfp4_group_gemm over the same groups with MXFP4 operands
 Weights are pre-quantized once, untimed, by the library's own quantizer.
 
 Prints one JSON line (rank 0). `value` is microseconds per call over the whole
@@ -45,8 +46,15 @@ WORKLOADS = {
     "medium": wl.MEDIUM,
     "compute": wl.COMPUTE,
     "nvfp4_grouped": wl.NVFP4_GROUPED,
+    "mxfp4_grouped": wl.MXFP4_GROUPED,
 }
-DEFAULT_STEPS = {"decode": 20000, "tiny": 20000, "medium": 10000, "compute": 50, "nvfp4_grouped": 500}
+DEFAULT_STEPS = {"decode": 20000, "tiny": 20000, "medium": 10000, "compute": 50, "nvfp4_grouped": 500,
+                 "mxfp4_grouped": 500}
+
+
+def grouped(name):
+    """Whether a workload is a grouped GEMM (NVFP4 or MXFP4)."""
+    return isinstance(WORKLOADS[name], wl.NVWorkload)
 
 
 def max_over_ranks(value, world, device):
@@ -311,27 +319,37 @@ def _cuda_memcpy_async():
 
 
 class NVCase:
-    """Grouped NVFP4 workload: operands quantized once (untimed) by nvfp4_quantize."""
+    """Grouped workload (NVFP4, or MXFP4 when w.vec == 32): operands quantized
+    once (untimed) by nvfp4_quantize / mxfp4_quantize."""
 
     def __init__(self, w, dev, mx, torch):
         self.w, self.mx, self.torch = w, mx, torch
+        nv = w.vec == 16
+        quant = mx.nvfp4_quantize if nv else mx.mxfp4_quantize
         to = lambda bits: torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
         self.groups = []
         for g in range(len(w.Ms)):
             a_bits, b_bits = wl.gen_nv_group(w, g)
-            qa, sfa = mx.nvfp4_quantize(to(a_bits))
-            qb, sfb = mx.nvfp4_quantize(to(b_bits))
-            c = torch.empty((w.Ms[g], w.N), dtype=torch.float16, device=dev)
+            qa, sfa = quant(to(a_bits))
+            qb, sfb = quant(to(b_bits))
+            c = torch.empty((w.Ms[g], w.N), dtype=torch.float16 if nv else torch.bfloat16, device=dev)
             self.groups.append(dict(a=qa, sfa=sfa, b=qb, sfb=sfb, c=c, k=w.K))
         torch.cuda.synchronize()
-        self.problems = mx.make_nv_problems(self.groups)
-        self.rot = 1                # 178 MB of operands per call already exceed twice the L2
+        if nv:
+            self.problems = mx.make_nv_problems(self.groups)
+            self.call = mx.nvfp4_group_gemm
+            plan = mx.nvfp4_group_gemm_plan(self.problems)
+        else:
+            self.problems = mx.make_mx_problems(self.groups)
+            self.call = mx.mxfp4_group_gemm
+            plan = mx.mxfp4_group_gemm_plan(self.problems)
+        self.rot = 1                # ~170 MB of operands per call already exceed twice the L2
         self.launches_per_step = 1
-        self.kernel_label, self.kernel_files = kernel_of(mx.nvfp4_group_gemm_plan(self.problems), "mxf4nvf4")
+        self.kernel_label, self.kernel_files = kernel_of(plan, "mxf4nvf4" if nv else "mxf4")
         self.rot_bytes = w.alg_bytes
 
     def step(self, i):
-        self.mx.nvfp4_group_gemm(self.groups, self.problems)
+        self.call(self.groups, self.problems)
 
     def alg_bytes(self):
         return self.w.alg_bytes
@@ -346,7 +364,7 @@ class NVCase:
             for (pa, ps), g in zip(pins_in, self.groups):
                 g["a"].copy_(pa, non_blocking=True)
                 g["sfa"].copy_(ps, non_blocking=True)
-            self.mx.nvfp4_group_gemm(self.groups, self.problems)
+            self.call(self.groups, self.problems)
             for po, g in zip(pins_out, self.groups):
                 po.copy_(g["c"], non_blocking=True)
 
@@ -373,7 +391,7 @@ def run_ours(args, name, rank, world, local_rank):
     w = WORKLOADS[name]
     steps = args.steps if args.steps is not None else DEFAULT_STEPS[name]
     warmup = args.warmup if args.warmup is not None else max(3, min(100, steps // 10))
-    case = NVCase(w, dev, mx, torch) if name == "nvfp4_grouped" else MXCase(w, dev, mx, torch)
+    case = NVCase(w, dev, mx, torch) if grouped(name) else MXCase(w, dev, mx, torch)
 
     for i in range(max(warmup, case.rot)):  # warm-up (also encodes every TMA descriptor once)
         case.step(i)
@@ -475,7 +493,7 @@ def run_ours(args, name, rank, world, local_rank):
         line["kernels_us"] = {k: round(v, 3) for k, v in split_times.items()}
 
     if not args.no_e2e:
-        short = case.launches_per_step == 1 and name != "nvfp4_grouped"
+        short = case.launches_per_step == 1 and not grouped(name)
         e2e_steps = max(10, min(steps, 2000 if short else 20))
         e_us, h2d, d2h = case.e2e(e2e_steps, torch)
         e_us = max_over_ranks(e_us, world, dev) / world
@@ -498,11 +516,12 @@ def _oracle_prep(name):
     if name in _ORACLE_PREP:
         return _ORACLE_PREP[name]
     w = WORKLOADS[name]
-    if name == "nvfp4_grouped":
+    if grouped(name):
+        quant = oracle.nv_quantize if w.vec == 16 else oracle.mx_quantize
         prep = []
         for g in range(len(w.Ms)):
             a_bits, b_bits = wl.gen_nv_group(w, g)
-            qb, sfb = oracle.nv_quantize(b_bits)
+            qb, sfb = quant(b_bits)
             prep.append((a_bits, qb, sfb))
     else:
         a_bits = wl.gen_a(w) if w.M <= 4096 else wl.gen_a(w, M=64)
@@ -516,13 +535,14 @@ def oracle_call_sampled(name, budget_s):
     """Time the oracle on a bounded sample of one call; return (us per full call, sample text)."""
     import oracle
     w = WORKLOADS[name]
-    if name == "nvfp4_grouped":
+    if grouped(name):
         # sample: the first r rows of every group, all N columns
+        quant = oracle.nv_quantize if w.vec == 16 else oracle.mx_quantize
         prep = _oracle_prep(name)
         t0 = time.perf_counter()
         a_bits, qb, sfb = prep[0]
-        qa, sfa = oracle.nv_quantize(a_bits[:1])
-        oracle.gemm_sampled(qa, sfa, qb, sfb, w.K, 16, np.zeros(w.N, np.int64), np.arange(w.N))
+        qa, sfa = quant(a_bits[:1])
+        oracle.gemm_sampled(qa, sfa, qb, sfb, w.K, w.vec, np.zeros(w.N, np.int64), np.arange(w.N))
         per_row = time.perf_counter() - t0
         total_rows = sum(w.Ms)
         r = max(1, min(max(w.Ms), int(budget_s / per_row / len(w.Ms))))
@@ -530,10 +550,10 @@ def oracle_call_sampled(name, budget_s):
         done_rows = 0
         for a_bits, qb, sfb in prep:
             rr = min(r, a_bits.shape[0])
-            qa, sfa = oracle.nv_quantize(a_bits[:rr])
+            qa, sfa = quant(a_bits[:rr])
             rows = np.repeat(np.arange(rr), w.N)
             cols = np.tile(np.arange(w.N), rr)
-            oracle.gemm_sampled(qa, sfa, qb, sfb, w.K, 16, rows, cols)
+            oracle.gemm_sampled(qa, sfa, qb, sfb, w.K, w.vec, rows, cols)
             done_rows += rr
         dt = time.perf_counter() - t0
         return (dt / done_rows * total_rows * 1e6,

@@ -284,6 +284,101 @@ mxfp4_status_t run_gemm(const void *Aq, int64_t ldaq, const void *A_sf, const vo
     return cuda_status(launch_gemm_mx(h, gp.bn, gp.splits, part, tickets, stream));
 }
 
+// ------------------------------------------------------------ grouped GEMMs
+// nvfp4_group_gemm (E4M3 per 16, fp16 C) and mxfp4_group_gemm (E8M0 per 32,
+// bf16 C) share the validation, the tensor maps and the kernel choice.
+template <typename Problem>
+mxfp4_status_t check_groups(const Problem *problems, int num_groups, int vec, bool pointers, int64_t *tiles,
+                            int64_t *pair_tile_count)
+{
+    if (!problems || num_groups < 1) return MXFP4_ERR_INVALID_ARG;
+    if (num_groups > kMaxGroups) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+    const int bn = gemm_block_n_nv();
+    *tiles = 0;
+    *pair_tile_count = 0;
+    for (int g = 0; g < num_groups; ++g) {
+        const Problem &p = problems[g];
+        if (pointers && (!p.a || !p.sfa || !p.b || !p.sfb || !p.c)) return MXFP4_ERR_INVALID_ARG;
+        if (p.m < 1 || p.n < 1 || p.k < 1 || p.m > kMaxDim || p.n > kMaxDim || p.k > kMaxDim)
+            return MXFP4_ERR_INVALID_ARG;
+        if (p.k % vec != 0) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+        if (pointers) {
+            if (p.lda < p.k / 2 || p.ldb < p.k / 2 || p.ldc < p.n) return MXFP4_ERR_INVALID_ARG;
+            if (p.lda % 16 != 0 || p.ldb % 16 != 0) return MXFP4_ERR_MISALIGNED;
+            if (!al16(p.a) || !al16(p.sfa) || !al16(p.b) || !al16(p.sfb) || !al2(p.c)) return MXFP4_ERR_MISALIGNED;
+        }
+        *tiles += ((p.m + 127) / 128) * ((p.n + bn - 1) / bn);
+        *pair_tile_count += pair_tiles(p.m, p.n);
+    }
+    if (*tiles > kMaxDim) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+    return MXFP4_OK;
+}
+
+template <typename Problem>
+mxfp4_status_t group_gemm(const Problem *problems, int num_groups, bool nv, void *stream)
+{
+    const int vec = nv ? 16 : 32;
+    int64_t tiles = 0, pair_tile_count = 0;
+    mxfp4_status_t st = check_groups(problems, num_groups, vec, true, &tiles, &pair_tile_count);
+    if (st != MXFP4_OK) return st;
+    const bool pair = use_pair(pair_tile_count);
+    int sms = 0;
+    st = current_device(&sms);
+    if (st != MXFP4_OK) return st;
+    GemmProblemHost hp[kMaxGroups];
+    memset(hp, 0, sizeof(hp));
+    const int bn = gemm_block_n_nv();
+    for (int g = 0; g < num_groups; ++g) {
+        const Problem &p = problems[g];
+        st = fp4_map(p.a, p.k / 2, p.m, p.lda, 128, &hp[g].tma);
+        if (st != MXFP4_OK) return st;
+        st = fp4_map(p.b, p.k / 2, p.n, p.ldb, pair ? 128 : bn, &hp[g].tmb);
+        if (st != MXFP4_OK) return st;
+        if (pair) {
+            st = sf_map(p.sfa, static_cast<int64_t>(sf_bytes(p.m, p.k, vec) / 512), pair_sf_box_blocks(nv),
+                        &hp[g].tmsfa);
+            if (st != MXFP4_OK) return st;
+            st = sf_map(p.sfb, static_cast<int64_t>(sf_bytes(p.n, p.k, vec) / 512), pair_sf_box_blocks(nv),
+                        &hp[g].tmsfb);
+            if (st != MXFP4_OK) return st;
+        }
+        hp[g].sfa = static_cast<const uint8_t *>(p.sfa);
+        hp[g].sfb = static_cast<const uint8_t *>(p.sfb);
+        hp[g].c = p.c;
+        hp[g].ldc = p.ldc;
+        hp[g].m = static_cast<int>(p.m);
+        hp[g].n = static_cast<int>(p.n);
+        hp[g].k = static_cast<int>(p.k);
+    }
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (nv)
+        return cuda_status(pair ? launch_gemm_nv_grouped_pair(hp, num_groups, s)
+                                : launch_gemm_nv_grouped(hp, num_groups, s));
+    return cuda_status(pair ? launch_gemm_mx_grouped_pair(hp, num_groups, s)
+                            : launch_gemm_mx_grouped(hp, num_groups, s));
+}
+
+template <typename Problem>
+mxfp4_status_t group_gemm_plan(const Problem *problems, int num_groups, bool nv, mxfp4_plan_t *out)
+{
+    if (!out) return MXFP4_ERR_INVALID_ARG;
+    int64_t tiles = 0, pair_tile_count = 0;
+    mxfp4_status_t st = check_groups(problems, num_groups, nv ? 16 : 32, false, &tiles, &pair_tile_count);
+    if (st != MXFP4_OK) return st;
+    int sms = 0;
+    st = current_device(&sms);
+    if (st != MXFP4_OK) return st;
+    memset(out, 0, sizeof(*out));
+    const bool pair = use_pair(pair_tile_count);
+    out->kernel = pair ? MXFP4_KERNEL_GEMM_PAIR : MXFP4_KERNEL_GEMM;
+    out->tile_m = pair ? 256 : 128;
+    out->tile_n = pair ? 256 : gemm_block_n_nv();
+    out->splits = 1;
+    out->tiles = static_cast<int>(pair ? pair_tile_count : tiles);
+    out->quant_launch = 0;
+    return MXFP4_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -401,51 +496,12 @@ mxfp4_status_t nvfp4_group_gemm(const nvfp4_problem_t *problems, int num_groups,
 {
     (void)workspace;
     (void)ws_bytes;
-    if (!problems || num_groups < 1) return MXFP4_ERR_INVALID_ARG;
-    if (num_groups > NVFP4_MAX_GROUPS) return MXFP4_ERR_UNSUPPORTED_SHAPE;
-    GemmProblemHost hp[kMaxGroups];
-    memset(hp, 0, sizeof(hp));
-    int64_t total_tiles = 0, total_pair_tiles = 0;
-    const int bn = gemm_block_n_nv();
-    for (int g = 0; g < num_groups; ++g) {
-        const nvfp4_problem_t &p = problems[g];
-        if (!p.a || !p.sfa || !p.b || !p.sfb || !p.c) return MXFP4_ERR_INVALID_ARG;
-        if (p.m < 1 || p.n < 1 || p.k < 1 || p.m > kMaxDim || p.n > kMaxDim || p.k > kMaxDim)
-            return MXFP4_ERR_INVALID_ARG;
-        if (p.k % 16 != 0) return MXFP4_ERR_UNSUPPORTED_SHAPE;
-        if (p.lda < p.k / 2 || p.ldb < p.k / 2 || p.ldc < p.n) return MXFP4_ERR_INVALID_ARG;
-        if (p.lda % 16 != 0 || p.ldb % 16 != 0) return MXFP4_ERR_MISALIGNED;
-        if (!al16(p.a) || !al16(p.sfa) || !al16(p.b) || !al16(p.sfb) || !al2(p.c)) return MXFP4_ERR_MISALIGNED;
-        total_tiles += ((p.m + 127) / 128) * ((p.n + bn - 1) / bn);
-        total_pair_tiles += pair_tiles(p.m, p.n);
-    }
-    if (total_tiles > kMaxDim) return MXFP4_ERR_UNSUPPORTED_SHAPE;
-    const bool pair = use_pair(total_pair_tiles);
-    int sms = 0;
-    mxfp4_status_t st = current_device(&sms);
-    if (st != MXFP4_OK) return st;
-    for (int g = 0; g < num_groups; ++g) {
-        const nvfp4_problem_t &p = problems[g];
-        st = fp4_map(p.a, p.k / 2, p.m, p.lda, 128, &hp[g].tma);
-        if (st != MXFP4_OK) return st;
-        st = fp4_map(p.b, p.k / 2, p.n, p.ldb, pair ? 128 : bn, &hp[g].tmb);
-        if (st != MXFP4_OK) return st;
-        if (pair) {
-            st = sf_map(p.sfa, static_cast<int64_t>(sf_bytes(p.m, p.k, 16) / 512), 4, &hp[g].tmsfa);
-            if (st != MXFP4_OK) return st;
-            st = sf_map(p.sfb, static_cast<int64_t>(sf_bytes(p.n, p.k, 16) / 512), 4, &hp[g].tmsfb);
-            if (st != MXFP4_OK) return st;
-        }
-        hp[g].sfa = static_cast<const uint8_t *>(p.sfa);
-        hp[g].sfb = static_cast<const uint8_t *>(p.sfb);
-        hp[g].c = p.c;
-        hp[g].ldc = p.ldc;
-        hp[g].m = static_cast<int>(p.m);
-        hp[g].n = static_cast<int>(p.n);
-        hp[g].k = static_cast<int>(p.k);
-    }
-    if (pair) return cuda_status(launch_gemm_nv_grouped_pair(hp, num_groups, static_cast<cudaStream_t>(stream)));
-    return cuda_status(launch_gemm_nv_grouped(hp, num_groups, static_cast<cudaStream_t>(stream)));
+    return group_gemm(problems, num_groups, true, stream);
+}
+
+mxfp4_status_t mxfp4_group_gemm(const mxfp4_problem_t *problems, int num_groups, void *stream)
+{
+    return group_gemm(problems, num_groups, false, stream);
 }
 
 mxfp4_status_t mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, int which, mxfp4_plan_t *out)
@@ -479,30 +535,12 @@ mxfp4_status_t mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, int which, mxfp4
 
 mxfp4_status_t nvfp4_group_gemm_plan(const nvfp4_problem_t *problems, int num_groups, mxfp4_plan_t *out)
 {
-    if (!out || !problems || num_groups < 1) return MXFP4_ERR_INVALID_ARG;
-    if (num_groups > NVFP4_MAX_GROUPS) return MXFP4_ERR_UNSUPPORTED_SHAPE;
-    int64_t tiles = 0, pair_tile_count = 0;
-    const int bn = gemm_block_n_nv();
-    for (int g = 0; g < num_groups; ++g) {
-        const nvfp4_problem_t &p = problems[g];
-        if (p.m < 1 || p.n < 1 || p.k < 1 || p.m > kMaxDim || p.n > kMaxDim || p.k > kMaxDim)
-            return MXFP4_ERR_INVALID_ARG;
-        if (p.k % 16 != 0) return MXFP4_ERR_UNSUPPORTED_SHAPE;
-        tiles += ((p.m + 127) / 128) * ((p.n + bn - 1) / bn);
-        pair_tile_count += pair_tiles(p.m, p.n);
-    }
-    int sms = 0;
-    const mxfp4_status_t st = current_device(&sms);
-    if (st != MXFP4_OK) return st;
-    memset(out, 0, sizeof(*out));
-    const bool pair = use_pair(pair_tile_count);
-    out->kernel = pair ? MXFP4_KERNEL_GEMM_PAIR : MXFP4_KERNEL_GEMM;
-    out->tile_m = pair ? 256 : 128;
-    out->tile_n = pair ? 256 : bn;
-    out->splits = 1;
-    out->tiles = static_cast<int>(pair ? pair_tile_count : tiles);
-    out->quant_launch = 0;
-    return MXFP4_OK;
+    return group_gemm_plan(problems, num_groups, true, out);
+}
+
+mxfp4_status_t mxfp4_group_gemm_plan(const mxfp4_problem_t *problems, int num_groups, mxfp4_plan_t *out)
+{
+    return group_gemm_plan(problems, num_groups, false, out);
 }
 
 mxfp4_status_t mxfp4_get_device_error(int *code)

@@ -495,6 +495,20 @@ cudaError_t launch_gemm_nv_grouped(const GemmProblemHost *probs, int num_groups,
     return launch_bs_gemm<1, kNvBN, kNvStages, kMaxGroups, true>(P, stream);
 }
 
+cudaError_t launch_gemm_mx_grouped(const GemmProblemHost *probs, int num_groups, cudaStream_t stream)
+{
+    GemmParams<kMaxGroups> P;
+    memset(&P, 0, sizeof(P));
+    int tiles = 0;
+    for (int g = 0; g < num_groups; ++g) fill_problem(P, g, probs[g], kNvBN, 32, tiles);
+    P.num_groups = num_groups;
+    P.total_tiles = tiles;
+    P.splits = 1;
+    P.partials = nullptr;
+    P.tickets = nullptr;
+    return launch_bs_gemm<0, kNvBN, kMxStages, kMaxGroups, false>(P, stream);
+}
+
 int read_and_clear_gemm_error()
 {
     int v = 0, zero = 0;

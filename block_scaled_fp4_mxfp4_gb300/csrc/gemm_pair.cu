@@ -425,6 +425,9 @@ cudaError_t launch_pair(const PairParams<MAXG> &params, cudaStream_t stream)
 
 constexpr int kPairMxStages = 6;   // 35 KB stages
 constexpr int kPairNvStages = 5;   // 38 KB stages; TMEM holds 5 stages of NVFP4 scales
+static_assert(PairCfg<0, kPairMxStages>::SF_BLK == pair_sf_box_blocks(false) &&
+                  PairCfg<1, kPairNvStages>::SF_BLK == pair_sf_box_blocks(true),
+              "scale tensor-map boxes are one stage of scale blocks");
 
 // Pair tiles: 256 rows of A (two CTAs) x 256 columns.
 template <int MAXG>
@@ -474,6 +477,17 @@ cudaError_t launch_gemm_nv_grouped_pair(const GemmProblemHost *probs, int num_gr
     P.num_groups = num_groups;
     P.total_tiles = tiles;
     return launch_pair<1, kPairNvStages, kMaxGroups, true>(P, stream);
+}
+
+cudaError_t launch_gemm_mx_grouped_pair(const GemmProblemHost *probs, int num_groups, cudaStream_t stream)
+{
+    PairParams<kMaxGroups> P;
+    memset(&P, 0, sizeof(P));
+    int tiles = 0;
+    for (int g = 0; g < num_groups; ++g) fill_pair_problem(P, g, probs[g], 32, tiles);
+    P.num_groups = num_groups;
+    P.total_tiles = tiles;
+    return launch_pair<0, kPairMxStages, kMaxGroups, false>(P, stream);
 }
 
 int read_and_clear_gemm_pair_error()

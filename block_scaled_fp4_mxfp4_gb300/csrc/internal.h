@@ -43,6 +43,9 @@ cudaError_t launch_gemm_mx(const GemmProblemHost &prob, int bn, int splits, floa
 // Grouped NVFP4 (kind::mxf4nvf4, fp16 C), one launch over all groups.
 cudaError_t launch_gemm_nv_grouped(const GemmProblemHost *probs, int num_groups,
                                    cudaStream_t stream);
+// Grouped MXFP4 (kind::mxf4, bf16 C), one launch over all groups.
+cudaError_t launch_gemm_mx_grouped(const GemmProblemHost *probs, int num_groups,
+                                   cudaStream_t stream);
 int read_and_clear_gemm_error();
 
 // ------------------------------------------------------------ gemm_pair.cu
@@ -50,8 +53,12 @@ int read_and_clear_gemm_error();
 // split-K) for problems with enough tiles to fill the GPU. prob.tmb boxes are
 // 128 rows (each CTA loads half of a tile's B).
 int pair_tiles(int64_t m, int64_t n);   // 256 x 256 tiles of an m x n output
+// scale blocks per tmsfa / tmsfb box (one stage): 2 for MXFP4, 4 for NVFP4
+constexpr int pair_sf_box_blocks(bool nvfp4) { return nvfp4 ? 4 : 2; }
 cudaError_t launch_gemm_mx_pair(const GemmProblemHost &prob, cudaStream_t stream);
 cudaError_t launch_gemm_nv_grouped_pair(const GemmProblemHost *probs, int num_groups,
+                                        cudaStream_t stream);
+cudaError_t launch_gemm_mx_grouped_pair(const GemmProblemHost *probs, int num_groups,
                                         cudaStream_t stream);
 int read_and_clear_gemm_pair_error();
 

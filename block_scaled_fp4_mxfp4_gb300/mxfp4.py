@@ -42,6 +42,11 @@ class NvProblem(ctypes.Structure):
                 ("lda", _i64), ("ldb", _i64), ("ldc", _i64)]
 
 
+class MxProblem(ctypes.Structure):
+    """mxfp4_problem_t (same fields as nvfp4_problem_t)."""
+    _fields_ = NvProblem._fields_
+
+
 class Plan(ctypes.Structure):
     """mxfp4_plan_t: the kernel and tiling a call launches."""
     _fields_ = [("kernel", ctypes.c_int), ("tile_m", ctypes.c_int), ("tile_n", ctypes.c_int),
@@ -87,6 +92,10 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.mxfp4_gemm_plan.argtypes = [_i64, _i64, _i64, ctypes.c_int, ctypes.POINTER(Plan)]
     L.nvfp4_group_gemm_plan.restype = _st
     L.nvfp4_group_gemm_plan.argtypes = [ctypes.POINTER(NvProblem), ctypes.c_int, ctypes.POINTER(Plan)]
+    L.mxfp4_group_gemm.restype = _st
+    L.mxfp4_group_gemm.argtypes = [ctypes.POINTER(MxProblem), ctypes.c_int, _p]
+    L.mxfp4_group_gemm_plan.restype = _st
+    L.mxfp4_group_gemm_plan.argtypes = [ctypes.POINTER(MxProblem), ctypes.c_int, ctypes.POINTER(Plan)]
     return L
 
 
@@ -221,17 +230,39 @@ def mxfp4_quant_gemm_fused(A, Bq, B_sf, C=None, workspace=None, stream=None):
     return C
 
 
-def make_nv_problems(groups):
-    """ctypes array of nvfp4_problem_t from dicts with keys a, sfa, b, sfb, c, k."""
-    arr = (NvProblem * len(groups))()
+def make_nv_problems(groups, struct=None):
+    """ctypes array of nvfp4_problem_t (or `struct`) from dicts with keys a, sfa,
+    b, sfb, c, k."""
+    struct = struct or NvProblem
+    arr = (struct * len(groups))()
     for i, g in enumerate(groups):
         a, b, c = g["a"], g["b"], g["c"]
         for name, t in (("a", a), ("b", b), ("c", c), ("sfa", g["sfa"]), ("sfb", g["sfb"])):
             _dev(t, name)
-        arr[i] = NvProblem(a.shape[0], b.shape[0], g["k"], a.data_ptr(), g["sfa"].data_ptr(),
+        arr[i] = struct(a.shape[0], b.shape[0], g["k"], a.data_ptr(), g["sfa"].data_ptr(),
                            b.data_ptr(), g["sfb"].data_ptr(), c.data_ptr(),
                            a.stride(0), b.stride(0), c.stride(0))
     return arr
+
+
+def make_mx_problems(groups):
+    """ctypes array of mxfp4_problem_t from dicts with keys a, sfa, b, sfb, c, k."""
+    return make_nv_problems(groups, MxProblem)
+
+
+def mxfp4_group_gemm(groups, problems=None, stream=None):
+    """Grouped MXFP4 GEMM (bf16 C) over `groups` (see make_mx_problems); returns the C list."""
+    if problems is None:
+        problems = make_mx_problems(groups)
+    _check(_lib.mxfp4_group_gemm(problems, len(problems), _stream_ptr(stream)), "mxfp4_group_gemm")
+    return [g["c"] for g in groups]
+
+
+def mxfp4_group_gemm_plan(problems) -> dict:
+    """What mxfp4_group_gemm launches for these problems (see make_mx_problems)."""
+    p = Plan()
+    _check(lib().mxfp4_group_gemm_plan(problems, len(problems), ctypes.byref(p)), "mxfp4_group_gemm_plan")
+    return _plan_dict(p)
 
 
 def nvfp4_group_gemm(groups, problems=None, stream=None):

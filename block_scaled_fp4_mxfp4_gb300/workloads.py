@@ -102,12 +102,14 @@ class MXWorkload:
 
 @dataclass
 class NVWorkload:
-    """Grouped NVFP4 GEMM: per group g, A_g [M_g, K] and B_g [N, K] E2M1 with E4M3 per 16."""
+    """Grouped GEMM: per group g, A_g [M_g, K] and B_g [N, K] E2M1 with a scale per
+    `vec` elements (16: E4M3, NVFP4, fp16 C; 32: E8M0, MXFP4, bf16 C)."""
     name: str
     Ms: list = field(default_factory=list)
     N: int = 0
     K: int = 0
     seed: int = 0
+    vec: int = 16
 
     @property
     def flops(self) -> int:
@@ -115,10 +117,10 @@ class NVWorkload:
 
     @property
     def alg_bytes(self) -> int:
-        """Packed A and B + their E4M3 scales + fp16 C, summed over groups."""
+        """Packed A and B + their scales + 16-bit C, summed over groups."""
         t = 0
         for m in self.Ms:
-            t += (m + self.N) * self.K // 2 + (m + self.N) * self.K // 16 + 2 * m * self.N
+            t += (m + self.N) * self.K // 2 + (m + self.N) * self.K // self.vec + 2 * m * self.N
         return t
 
 
@@ -128,6 +130,10 @@ MEDIUM = MXWorkload("mxfp4_medium_heavytail_M256_N7168_K2048", 256, 7168, 2048, 
 COMPUTE = MXWorkload("mxfp4_compute_M8192_N8192_K8192", 8192, 8192, 8192, "uniform4", 1.0, 1.0)
 NVFP4_GROUPED = NVWorkload("nvfp4_grouped_8x_N4096_K7168",
                            [64, 128, 256, 384, 512, 640, 768, 1024], 4096, 7168)
+# The same grouped shapes with MXFP4 operands (E8M0 per 32, bf16 C): the grouped
+# MXFP4 (mixture-of-experts) GEMM beyond the pages' single-problem MXFP4 call.
+MXFP4_GROUPED = NVWorkload("mxfp4_grouped_8x_N4096_K7168",
+                           [64, 128, 256, 384, 512, 640, 768, 1024], 4096, 7168, vec=32)
 
 MX_WORKLOADS = {w.name: w for w in (TINY, DECODE, MEDIUM, COMPUTE)}
 

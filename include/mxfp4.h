@@ -187,6 +187,31 @@ MXFP4_API size_t nvfp4_group_workspace_bytes(int num_groups);
 MXFP4_API mxfp4_status_t nvfp4_group_gemm(const nvfp4_problem_t *problems, int num_groups, void *workspace,
                                 size_t ws_bytes, void *stream);
 
+/* One problem of a grouped MXFP4 GEMM: the problem list of [NV-496271]
+ * custom_kernel (a, b, c, their scales, (m, n, k)) with MXFP4 operands
+ * ([MM-517169]: E2M1 codes, E8M0 scale per 32 along K) and bf16 C, the layout
+ * of a mixture-of-experts layer whose experts hold MXFP4 weights. */
+typedef struct {
+    int64_t m, n, k;   /* C is [m, n]; k is the reduction length (multiple of 32) */
+    const void *a;     /* uint8 [m, k/2] packed E2M1, row stride lda bytes */
+    const void *sfa;   /* blocked E8M0 scales, mxfp4_sf_bytes(m, k, 32) bytes */
+    const void *b;     /* uint8 [n, k/2] packed E2M1, row stride ldb bytes */
+    const void *sfb;   /* blocked E8M0 scales, mxfp4_sf_bytes(n, k, 32) bytes */
+    void *c;           /* out: bf16 [m, n], row stride ldc elements */
+    int64_t lda, ldb, ldc;
+} mxfp4_problem_t;
+
+/* Maximum number of problems in one mxfp4_group_gemm call. */
+#define MXFP4_MAX_GROUPS 16
+
+/* Grouped MXFP4 GEMM: for each problem g,
+ *   C_g[m, n] = bf16_rne( sum_k e2m1(a[m,k]) 2^(sfa[m,k/32]-127) e2m1(b[n,k]) 2^(sfb[n,k/32]-127) )
+ * with fp32 accumulation (tcgen05.mma kind::mxf4, scale_vec::2X), all groups
+ * in ONE launch scheduled tile by tile, as nvfp4_group_gemm does for NVFP4.
+ * `problems` is a host array of num_groups entries (1 <= num_groups <=
+ * MXFP4_MAX_GROUPS), read during the call only. Needs no workspace. */
+MXFP4_API mxfp4_status_t mxfp4_group_gemm(const mxfp4_problem_t *problems, int num_groups, void *stream);
+
 /* Bytes of the fixed device scratch array behind mxfp4_gemm_a4w4_noalloc
  * (8 MiB). */
 MXFP4_API size_t mxfp4_noalloc_scratch_bytes(void);
@@ -240,8 +265,11 @@ typedef struct {
  * GB300). Argument checks as for the calls themselves, minus the pointers. */
 MXFP4_API mxfp4_status_t mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, int which, mxfp4_plan_t *out);
 
-/* The plan of nvfp4_group_gemm for these problems (pointers are not read). */
+/* The plan of nvfp4_group_gemm / mxfp4_group_gemm for these problems
+ * (pointers are not read). */
 MXFP4_API mxfp4_status_t nvfp4_group_gemm_plan(const nvfp4_problem_t *problems, int num_groups,
+                                               mxfp4_plan_t *out);
+MXFP4_API mxfp4_status_t mxfp4_group_gemm_plan(const mxfp4_problem_t *problems, int num_groups,
                                                mxfp4_plan_t *out);
 
 /* Reads and clears the library's device-side error word. Kernels never trap:

@@ -14,7 +14,7 @@ L = mxfp4.lib()
 
 def test_every_declared_symbol_is_exported():
     names = mxfp4.declared_symbols()
-    assert len(names) == 15
+    assert len(names) == 17
     for n in names:
         assert hasattr(L, n), n  # ctypes resolves the exported symbol
 
@@ -118,3 +118,22 @@ def test_plan_argument_validation_needs_no_gpu():
 def test_plan_without_gpu_reports_no_device():
     plan = mxfp4.Plan()
     assert L.mxfp4_gemm_plan(16, 2112, 7168, 1, ctypes.byref(plan)) == 7
+
+
+def test_mx_group_gemm_validation_needs_no_gpu():
+    P = mxfp4.MxProblem
+    good = (P * 1)()
+    good[0] = P(64, 256, 512, 16, 16, 16, 16, 16, 256, 256, 256)
+    bad_k = (P * 1)()
+    bad_k[0] = P(64, 256, 48, 16, 16, 16, 16, 16, 32, 32, 256)      # K % 32
+    assert L.mxfp4_group_gemm(bad_k, 1, None) == 2
+    null = (P * 1)()
+    null[0] = P(64, 256, 512, 0, 16, 16, 16, 16, 256, 256, 256)     # null A
+    assert L.mxfp4_group_gemm(null, 1, None) == 1
+    bad_al = (P * 1)()
+    bad_al[0] = P(64, 256, 512, 16, 16, 16, 16, 16, 264, 256, 256)  # lda % 16
+    assert L.mxfp4_group_gemm(bad_al, 1, None) == 3
+    assert L.mxfp4_group_gemm(good, 17, None) == 2                   # too many groups
+    assert L.mxfp4_group_gemm(None, 1, None) == 1
+    plan = mxfp4.Plan()
+    assert L.mxfp4_group_gemm_plan(bad_k, 1, ctypes.byref(plan)) == 2

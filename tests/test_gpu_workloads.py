@@ -106,3 +106,29 @@ def test_plans_of_the_benchmarked_calls():
     p = mx.nvfp4_group_gemm_plan(mx.make_nv_problems(groups))
     assert p["kernel"] == "bs_gemm_pair_kernel"
     assert p["tiles"] == sum((m + 255) // 256 for m in w.Ms) * (w.N // 256)
+
+
+def test_mxfp4_grouped_sampled():
+    w = wl.MXFP4_GROUPED
+    groups, refs = [], []
+    for g in range(len(w.Ms)):
+        a_bits, b_bits = wl.gen_nv_group(w, g)
+        qa, sfa = mx.mxfp4_quantize(dev_bf16(a_bits))
+        qb, sfb = mx.mxfp4_quantize(dev_bf16(b_bits))
+        c = torch.full((w.Ms[g], w.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        groups.append(dict(a=qa, sfa=sfa, b=qb, sfb=sfb, c=c, k=w.K))
+        refs.append((a_bits, b_bits))
+    problems = mx.make_mx_problems(groups)
+    assert mx.mxfp4_group_gemm_plan(problems)["kernel"] == "bs_gemm_pair_kernel"
+    mx.mxfp4_group_gemm(groups, problems)                 # the call bench.py times
+    torch.cuda.synchronize()
+    for g, (gd, (a_bits, b_bits)) in enumerate(zip(groups, refs)):
+        qa_r, sfa_r = oracle.mx_quantize(a_bits)
+        qb_r, sfb_r = oracle.mx_quantize(b_bits)
+        assert_bytes_equal(host(gd["a"]), qa_r, f"group {g} A codes")
+        assert_bytes_equal(host(gd["sfb"]), sfb_r, f"group {g} B scales")
+        rows, cols = sample_pairs(w.Ms[g], w.N, 2048, 1, 1, seed=60 + g)
+        c_ref, s = oracle.gemm_sampled(qa_r, sfa_r, qb_r, sfb_r, w.K, 32, rows, cols)
+        got = gd["c"][torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].float().cpu().numpy()
+        assert_within_tolerance(got.astype(np.float64), c_ref, s, f"mxfp4 group {g} (sampled)")
+    assert mx.get_device_error() == 0
