@@ -3,6 +3,7 @@
 // path selection. Nothing here allocates device memory or synchronizes.
 #include <cudaTypedefs.h>
 
+#include <cmath>
 #include <cstring>
 #include <mutex>
 #include <unordered_map>
@@ -253,12 +254,24 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K)
     return w;
 }
 
+// Optional GEMM epilogue (mxfp4_gemm_a4w4_ex): C = alpha * acc + beta * C + bias.
+struct Epilogue {
+    bool on;
+    float alpha, beta;
+    const void *bias;
+};
+constexpr Epilogue kNoEpilogue{false, 1.0f, 0.0f, nullptr};
+
 mxfp4_status_t run_gemm(const void *Aq, int64_t ldaq, const void *A_sf, const void *Bq, int64_t ldbq,
                         const void *B_sf, void *C, int64_t ldc, int64_t M, int64_t N, int64_t K, void *ws,
-                        const WsLayout &wl, cudaStream_t stream)
+                        const WsLayout &wl, cudaStream_t stream, const Epilogue &epi = kNoEpilogue)
 {
     GemmProblemHost h;
     memset(&h, 0, sizeof(h));
+    h.epi = epi.on;
+    h.alpha = epi.alpha;
+    h.beta = epi.beta;
+    h.bias = epi.bias;
     mxfp4_status_t st = fp4_map(Aq, K / 2, M, ldaq, 128, &h.tma);
     if (st != MXFP4_OK) return st;
     const GemmPlan gp = plan_gemm(M, N, K);
@@ -456,6 +469,28 @@ mxfp4_status_t mxfp4_gemm_a4w4(const void *Aq, int64_t ldaq, const void *A_sf, c
     if (st != MXFP4_OK) return st;
     return run_gemm(Aq, ldaq, A_sf, Bq, ldbq, B_sf, C, ldc, M, N, K, workspace, wl,
                     static_cast<cudaStream_t>(stream));
+}
+
+mxfp4_status_t mxfp4_gemm_a4w4_ex(const void *Aq, int64_t ldaq, const void *A_sf, const void *Bq, int64_t ldbq,
+                                  const void *B_sf, void *C, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                  float alpha, float beta, const void *bias, void *workspace, size_t ws_bytes,
+                                  void *stream)
+{
+    mxfp4_status_t st = check_gemm_common(Bq, ldbq, B_sf, C, ldc, M, N, K);
+    if (st != MXFP4_OK) return st;
+    if (!Aq || !A_sf || !workspace) return MXFP4_ERR_INVALID_ARG;
+    if (ldaq < K / 2) return MXFP4_ERR_INVALID_ARG;
+    if (!std::isfinite(alpha) || !std::isfinite(beta)) return MXFP4_ERR_INVALID_ARG;
+    if (ldaq % 16 != 0 || !al16(Aq) || !al16(A_sf) || !al16(workspace)) return MXFP4_ERR_MISALIGNED;
+    if (bias && !al2(bias)) return MXFP4_ERR_MISALIGNED;
+    const WsLayout wl = ws_layout(M, N, K);
+    if (ws_bytes < wl.total) return MXFP4_ERR_WORKSPACE_TOO_SMALL;
+    int sms = 0;
+    st = current_device(&sms);
+    if (st != MXFP4_OK) return st;
+    const Epilogue epi{!(alpha == 1.0f && beta == 0.0f && bias == nullptr), alpha, beta, bias};
+    return run_gemm(Aq, ldaq, A_sf, Bq, ldbq, B_sf, C, ldc, M, N, K, workspace, wl,
+                    static_cast<cudaStream_t>(stream), epi);
 }
 
 mxfp4_status_t mxfp4_quant_gemm_fused(const void *A, int64_t lda, const void *Bq, int64_t ldbq, const void *B_sf,

@@ -78,7 +78,9 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams<MAXG> &p, int u)
 //   warps 4-7      epilogue: drain the accumulator rows of a finished unit
 //                  into registers, hand TMEM back to the MMA issuer, then
 //                  write C while the next unit's mainloop runs
-template <int KIND, int BN, int STAGES, int MAXG, bool F16>
+// EPI: the variant with the alpha / beta / bias epilogue (mxfp4_gemm_a4w4_ex);
+// the plain variant keeps its registers for the common case.
+template <int KIND, int BN, int STAGES, int MAXG, bool F16, bool EPI = false>
 __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__ GemmParams<MAXG> p)
 {
     using Cfg = GemmCfg<KIND, BN, STAGES>;
@@ -311,7 +313,29 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
             tc_fence_after();
             const bool run = (*abort_flag == 0);
             const int row = w.m_tile * 128 + row_in_tile;
-            if (p.splits == 1) {
+            if (EPI && p.splits == 1 && pr.epi) {
+                // epilogue with alpha / beta / bias: each 32-column chunk is
+                // finished and stored straight from TMEM, then TMEM is released
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(t_row + c * 32, v);
+                    tmem_ld_wait();
+                    const int col0 = w.n_tile * BN + c * 32;
+                    if (run && row < pr.m && col0 < pr.n) {
+                        uint32_t part[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int ca = min(col0 + 2 * j, pr.n - 1), cb = min(col0 + 2 * j + 1, pr.n - 1);
+                            part[j] = pack2<F16>(epilogue_value<F16>(pr, __uint_as_float(v[2 * j]), row, ca),
+                                                 epilogue_value<F16>(pr, __uint_as_float(v[2 * j + 1]), row, cb));
+                        }
+                        store_packed32(pr.c, pr.ldc, row, col0, pr.n, part);
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(acc_empty);
+            } else if (p.splits == 1) {
                 // drain the row into registers, release TMEM, then store
                 uint32_t pk[BN / 2];
 #pragma unroll
@@ -373,6 +397,10 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
 #pragma unroll
                             for (int j = 0; j < 32; ++j) f[j] += __ldcg(qv + (c0 + j) * col_stride + row);
                         }
+                        if (EPI && pr.epi) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) f[j] = epilogue_value<F16>(pr, f[j], row, min(col0 + j, pr.n - 1));
+                        }
                         uint32_t pk[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) pk[j] = pack2<F16>(f[2 * j], f[2 * j + 1]);
@@ -402,11 +430,11 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
     }
 }
 
-template <int KIND, int BN, int STAGES, int MAXG, bool F16>
+template <int KIND, int BN, int STAGES, int MAXG, bool F16, bool EPI = false>
 cudaError_t launch_bs_gemm(const GemmParams<MAXG> &params, cudaStream_t stream)
 {
     using Cfg = GemmCfg<KIND, BN, STAGES>;
-    auto kern = bs_gemm_kernel<KIND, BN, STAGES, MAXG, F16>;
+    auto kern = bs_gemm_kernel<KIND, BN, STAGES, MAXG, F16, EPI>;
     static uint64_t configured = 0;  // one bit per device; setting it twice is harmless
     static int sms_of[64] = {};
     int dev = 0;
@@ -456,7 +484,10 @@ void fill_problem(GemmParams<MAXG> &P, int g, const GemmProblemHost &h, int bn, 
     d.n_tiles = (h.n + bn - 1) / bn;
     d.tile_start = tiles;
     d.sf_cblocks = (h.k / vec + 3) / 4;
-    d.pad_ = 0;
+    d.epi = h.epi ? 1 : 0;
+    d.alpha = h.alpha;
+    d.beta = h.beta;
+    d.bias = static_cast<const uint16_t *>(h.bias);
     tiles += d.m_tiles * d.n_tiles;
 }
 
@@ -477,6 +508,10 @@ cudaError_t launch_gemm_mx(const GemmProblemHost &prob, int bn, int splits, floa
     P.splits = splits;
     P.partials = partials;
     P.tickets = tickets;
+    if (prob.epi) {
+        if (bn == 128) return launch_bs_gemm<0, 128, kMxNarrowStages, 1, false, true>(P, stream);
+        return launch_bs_gemm<0, 256, kMxStages, 1, false, true>(P, stream);
+    }
     if (bn == 128) return launch_bs_gemm<0, 128, kMxNarrowStages, 1, false>(P, stream);
     return launch_bs_gemm<0, 256, kMxStages, 1, false>(P, stream);
 }

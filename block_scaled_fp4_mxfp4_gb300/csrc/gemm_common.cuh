@@ -19,7 +19,9 @@ struct GemmProblemDev {
     int m_tiles, n_tiles;
     int tile_start;
     int sf_cblocks;   // column blocks of 4 scales per 128-row chunk
-    int pad_;
+    int epi;          // nonzero: C = alpha * acc + beta * C + bias[col]
+    float alpha, beta;
+    const uint16_t *bias;   // [n] in C's type, or null
 };
 
 template <int MAXG>
@@ -73,6 +75,28 @@ __device__ __forceinline__ uint32_t pack2(float a, float b)
         __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
         return *reinterpret_cast<uint32_t *>(&h);
     }
+}
+
+template <bool F16>
+__device__ __forceinline__ float c_to_float(uint16_t v)
+{
+    if constexpr (F16)
+        return __half2float(__ushort_as_half(v));
+    else
+        return __uint_as_float(static_cast<uint32_t>(v) << 16);
+}
+
+// Output value of element (row, col) under the epilogue of pr: in fp32,
+// ((alpha * acc) + beta * C[row, col]) + bias[col], C read before it is
+// overwritten; beta = 0 leaves C unread and a null bias adds nothing.
+template <bool F16>
+__device__ __forceinline__ float epilogue_value(const GemmProblemDev &pr, float acc, int row, int col)
+{
+    float t = pr.alpha * acc;
+    if (pr.beta != 0.0f)
+        t += pr.beta * c_to_float<F16>(static_cast<const uint16_t *>(pr.c)[static_cast<int64_t>(row) * pr.ldc + col]);
+    if (pr.bias) t += c_to_float<F16>(pr.bias[col]);
+    return t;
 }
 
 // Stores 32 consecutive 16-bit C values of one row (16 packed pairs) at

@@ -97,7 +97,8 @@ __device__ __forceinline__ PairUnit decode_pair_unit(const PairParams<MAXG> &p, 
     return w;
 }
 
-template <int KIND, int STAGES, int MAXG, bool F16>
+// EPI: the variant with the alpha / beta / bias epilogue (mxfp4_gemm_a4w4_ex).
+template <int KIND, int STAGES, int MAXG, bool F16, bool EPI = false>
 __global__ void __launch_bounds__(256, 1) bs_gemm_pair_kernel(const __grid_constant__ PairParams<MAXG> p)
 {
     using Cfg = PairCfg<KIND, STAGES>;
@@ -338,6 +339,31 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_pair_kernel(const __grid_const
             tc_fence_after();
             const bool run = (*abort_flag == 0);
             const int row = w.m_pair * 256 + static_cast<int>(rank) * 128 + row_in_tile;
+            if (EPI && pr.epi) {
+                // epilogue with alpha / beta / bias: each 32-column chunk is
+                // finished and stored straight from TMEM, then TMEM goes back
+#pragma unroll 1
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(t_row + c * 32, v);
+                    tmem_ld_wait();
+                    const int col0 = w.n_tile * 256 + c * 32;
+                    if (run && row < pr.m && col0 < pr.n) {
+                        uint32_t part[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int ca = min(col0 + 2 * j, pr.n - 1), cb = min(col0 + 2 * j + 1, pr.n - 1);
+                            part[j] = pack2<F16>(epilogue_value<F16>(pr, __uint_as_float(v[2 * j]), row, ca),
+                                                 epilogue_value<F16>(pr, __uint_as_float(v[2 * j + 1]), row, cb));
+                        }
+                        store_packed32(pr.c, pr.ldc, row, col0, pr.n, part);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(acc_empty_r0);
+                continue;
+            }
             // drain the row into registers, hand TMEM back, then store
             uint32_t pk[128];
 #pragma unroll
@@ -387,11 +413,11 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_pair_kernel(const __grid_const
     }
 }
 
-template <int KIND, int STAGES, int MAXG, bool F16>
+template <int KIND, int STAGES, int MAXG, bool F16, bool EPI = false>
 cudaError_t launch_pair(const PairParams<MAXG> &params, cudaStream_t stream)
 {
     using Cfg = PairCfg<KIND, STAGES>;
-    auto kern = bs_gemm_pair_kernel<KIND, STAGES, MAXG, F16>;
+    auto kern = bs_gemm_pair_kernel<KIND, STAGES, MAXG, F16, EPI>;
     static uint64_t configured = 0;  // one bit per device; setting it twice is harmless
     static int sms_of[64] = {};
     int dev = 0;
@@ -449,7 +475,10 @@ void fill_pair_problem(PairParams<MAXG> &P, int g, const GemmProblemHost &h, int
     d.n_tiles = (h.n + 255) / 256;
     d.tile_start = tiles;
     d.sf_cblocks = (h.k / vec + 3) / 4;
-    d.pad_ = 0;
+    d.epi = h.epi ? 1 : 0;
+    d.alpha = h.alpha;
+    d.beta = h.beta;
+    d.bias = static_cast<const uint16_t *>(h.bias);
     tiles += d.m_tiles * d.n_tiles;
 }
 
@@ -465,6 +494,7 @@ cudaError_t launch_gemm_mx_pair(const GemmProblemHost &prob, cudaStream_t stream
     fill_pair_problem(P, 0, prob, 32, tiles);
     P.num_groups = 1;
     P.total_tiles = tiles;
+    if (prob.epi) return launch_pair<0, kPairMxStages, 1, false, true>(P, stream);
     return launch_pair<0, kPairMxStages, 1, false>(P, stream);
 }
 

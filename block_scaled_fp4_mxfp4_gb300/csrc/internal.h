@@ -26,6 +26,10 @@ struct GemmProblemHost {
     void *c;                  // bf16 (MXFP4) or fp16 (NVFP4) [m, n]
     int64_t ldc;              // elements
     int m, n, k;
+    // optional epilogue C = alpha * acc + beta * C + bias[n] (epi false: C = acc)
+    bool epi;
+    float alpha, beta;
+    const void *bias;         // [n] in C's type, or null
     // CTA-pair kernels only: the scale buffers as [blocks, 128 u32] with a box of
     // one stage's K-blocks (2 for MXFP4, 4 for NVFP4)
     CUtensorMap tmsfa;

@@ -78,6 +78,9 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
         f.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p, _p]
     L.mxfp4_gemm_a4w4.restype = _st
     L.mxfp4_gemm_a4w4.argtypes = [_p, _i64, _p, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p, _sz, _p]
+    L.mxfp4_gemm_a4w4_ex.restype = _st
+    L.mxfp4_gemm_a4w4_ex.argtypes = [_p, _i64, _p, _p, _i64, _p, _p, _i64, _i64, _i64, _i64,
+                                     ctypes.c_float, ctypes.c_float, _p, _p, _sz, _p]
     L.mxfp4_quant_gemm_fused.restype = _st
     L.mxfp4_quant_gemm_fused.argtypes = [_p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p, _sz, _p]
     L.nvfp4_group_gemm.restype = _st
@@ -195,6 +198,31 @@ def mxfp4_gemm_a4w4(Aq, A_sf, Bq, B_sf, K: int, C=None, workspace=None, stream=N
                                 Bq.stride(0), B_sf.data_ptr(), C.data_ptr(), C.stride(0), M, N, K,
                                 workspace.data_ptr(), workspace.numel(), _stream_ptr(stream)),
            "mxfp4_gemm_a4w4")
+    return C
+
+
+def mxfp4_gemm_a4w4_ex(Aq, A_sf, Bq, B_sf, K: int, C=None, alpha: float = 1.0, beta: float = 0.0,
+                       bias=None, workspace=None, stream=None):
+    """C = bf16(alpha * (A_q . B_q^T) + beta * C + bias[n]) (see include/mxfp4.h)."""
+    _dev(Aq, "Aq", torch.uint8, 2)
+    _dev(Bq, "Bq", torch.uint8, 2)
+    M, N = Aq.shape[0], Bq.shape[0]
+    if C is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs the input C")
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=Aq.device)
+    _dev(C, "C", torch.bfloat16, 2)
+    if bias is not None:
+        _dev(bias, "bias", torch.bfloat16, 1)
+        if bias.numel() != N:
+            raise ValueError(f"bias must have N = {N} elements")
+    if workspace is None:
+        workspace = new_workspace(M, N, K, Aq.device)
+    _check(_lib.mxfp4_gemm_a4w4_ex(Aq.data_ptr(), Aq.stride(0), A_sf.data_ptr(), Bq.data_ptr(), Bq.stride(0),
+                                   B_sf.data_ptr(), C.data_ptr(), C.stride(0), M, N, K, float(alpha), float(beta),
+                                   bias.data_ptr() if bias is not None else None, workspace.data_ptr(),
+                                   workspace.numel(), _stream_ptr(stream)),
+           "mxfp4_gemm_a4w4_ex")
     return C
 
 

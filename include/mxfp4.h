@@ -144,6 +144,19 @@ MXFP4_API mxfp4_status_t mxfp4_gemm_a4w4(const void *Aq, int64_t ldaq, const voi
                                int64_t N, int64_t K, void *workspace, size_t ws_bytes,
                                void *stream);
 
+/* mxfp4_gemm_a4w4 with the epilogue extras the source pages' GEMM call
+ * carries ([MM-683203] "Launch 2": bias, alpha, beta, there None / 1.0 / 0.0):
+ *   C[m, n] = bf16_rne( ((alpha * acc[m, n]) + beta * C[m, n]) + bias[n] )
+ * evaluated in fp32 in that order, where acc is the fp32 block-scaled product
+ * of mxfp4_gemm_a4w4 and C[m, n] on the right is C's value before the call
+ * (not read when beta == 0). bias: bf16 [N] (2-byte aligned) or NULL.
+ * alpha and beta must be finite. alpha = 1, beta = 0, bias = NULL is exactly
+ * mxfp4_gemm_a4w4. Same workspace as mxfp4_gemm_a4w4. */
+MXFP4_API mxfp4_status_t mxfp4_gemm_a4w4_ex(const void *Aq, int64_t ldaq, const void *A_sf, const void *Bq,
+                                            int64_t ldbq, const void *B_sf, void *C, int64_t ldc, int64_t M,
+                                            int64_t N, int64_t K, float alpha, float beta, const void *bias,
+                                            void *workspace, size_t ws_bytes, void *stream);
+
 /* Dynamic MXFP4 quantization of bf16 A fused with the block-scaled GEMM
  * against pre-quantized Bq ([MM-517169] "Optimization 5"; [MM-683203] docstring).
  * Result equals mxfp4_quantize(A) followed by mxfp4_gemm_a4w4 (bit-identical

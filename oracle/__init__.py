@@ -226,6 +226,29 @@ def gemm_sampled(qa, sfa, qb, sfb, K: int, vec: int, rows, cols):
     return c, s
 
 
+def gemm_epilogue(c_acc, s_abs, alpha: float, beta: float, c_in=None, bias=None):
+    """The GEMM call's epilogue extras (kernelbot-amd-mxfp4-mm-683203, the
+    hot-path "Launch 2" call passes bias, alpha and beta, there None, 1.0 and
+    0.0; the page gives no formula). Reading, the usual GEMM epilogue:
+        C[m, n] = alpha * acc[m, n] + beta * C_in[m, n] + bias[n]
+    in fp64 on the exact product `c_acc` (from gemm_full / gemm_sampled).
+    Returns (C_ref, S) for check_tolerance, with S = |alpha| * sum|a b| +
+    |beta * C_in| + |bias|: the contract's 2^-8 * S term grows by the terms the
+    epilogue adds to the value that is rounded to bf16.
+    c_in and bias are float arrays (bias broadcast over rows), or None."""
+    c = alpha * np.asarray(c_acc, dtype=np.float64)
+    S = abs(alpha) * np.asarray(s_abs, dtype=np.float64)
+    if beta != 0.0:
+        cin = np.asarray(c_in, dtype=np.float64)
+        c = c + beta * cin
+        S = S + np.abs(beta * cin)
+    if bias is not None:
+        b = np.asarray(bias, dtype=np.float64)
+        c = c + b
+        S = S + np.abs(b)
+    return c, S
+
+
 def check_tolerance(c_gpu, c_ref, s_abs):
     """Contract: |C_gpu - C_ref| <= 2^-8 * S + 1e-3 per element -> (n_bad, worst ratio)."""
     cg = np.ascontiguousarray(c_gpu, dtype=np.float64).ravel()

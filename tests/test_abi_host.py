@@ -14,7 +14,7 @@ L = mxfp4.lib()
 
 def test_every_declared_symbol_is_exported():
     names = mxfp4.declared_symbols()
-    assert len(names) == 17
+    assert len(names) == 18
     for n in names:
         assert hasattr(L, n), n  # ctypes resolves the exported symbol
 
@@ -137,3 +137,18 @@ def test_mx_group_gemm_validation_needs_no_gpu():
     assert L.mxfp4_group_gemm(None, 1, None) == 1
     plan = mxfp4.Plan()
     assert L.mxfp4_group_gemm_plan(bad_k, 1, ctypes.byref(plan)) == 2
+
+
+def test_gemm_ex_argument_validation_needs_no_gpu():
+    f = L.mxfp4_gemm_a4w4_ex
+    ok = dict(aq=16, ldaq=512, asf=16, bq=16, ldbq=512, bsf=16, c=16, ldc=64, M=8, N=64, K=1024,
+              alpha=1.0, beta=0.0, bias=None, ws=16, wsb=1 << 20)
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["aq"], a["ldaq"], a["asf"], a["bq"], a["ldbq"], a["bsf"], a["c"], a["ldc"], a["M"], a["N"],
+                 a["K"], a["alpha"], a["beta"], a["bias"], a["ws"], a["wsb"], None)
+    assert call(alpha=float("inf")) == 1
+    assert call(beta=float("nan")) == 1
+    assert call(bias=17) == 3          # bias must be 2-byte aligned
+    assert call(K=1000) == 2           # K % 32
+    assert call(ws=0) == 1

@@ -407,3 +407,43 @@ def test_tolerance_checker_bound():
     n, worst = oracle.check_tolerance(ref + [1.01, 0, 0], ref, s)
     assert n == 1 and worst > 1.0
     assert oracle.check_tolerance(ref + [np.nan, 0, 0], ref, s)[0] == 1
+
+
+# ------------------------------------------------------------ GEMM epilogue
+def _small_gemm(seed, M=5, N=7, K=64):
+    a = wl.gen_bf16(seed, 1, M, K)
+    b = wl.gen_bf16(seed, 2, N, K)
+    qa, sfa = oracle.mx_quantize(a)
+    qb, sfb = oracle.mx_quantize(b)
+    return oracle.gemm_full(qa, sfa, qb, sfb, K, 32)
+
+
+def test_epilogue_identity_is_the_plain_gemm():
+    c, s = _small_gemm(70)
+    c2, s2 = oracle.gemm_epilogue(c, s, 1.0, 0.0)
+    assert np.array_equal(c, c2) and np.array_equal(s, s2)
+
+
+def test_epilogue_with_zero_product_is_beta_c_plus_bias():
+    """A = 0: every code and scale is zero, the product vanishes and C is the
+    closed form beta * C_in + bias."""
+    M, N, K = 4, 6, 64
+    qa, sfa = oracle.mx_quantize(np.zeros((M, K), dtype=np.uint16))
+    qb, sfb = oracle.mx_quantize(wl.gen_bf16(71, 2, N, K))
+    c, s = oracle.gemm_full(qa, sfa, qb, sfb, K, 32)
+    assert np.all(c == 0.0)
+    c_in = np.arange(M * N, dtype=np.float64).reshape(M, N) - 7.5
+    bias = np.linspace(-2.0, 3.0, N)
+    out, S = oracle.gemm_epilogue(c, s, 3.0, -0.5, c_in, bias)
+    assert np.array_equal(out, -0.5 * c_in + bias[None, :])
+    assert np.array_equal(S, np.abs(0.5 * c_in) + np.abs(bias)[None, :])
+
+
+def test_epilogue_is_linear_in_alpha_and_beta():
+    c, s = _small_gemm(72)
+    c_in = wl.bf16_bits_to_float(wl.gen_bf16(72, 3, *c.shape)).astype(np.float64)
+    one, _ = oracle.gemm_epilogue(c, s, 1.0, 0.0)
+    two, _ = oracle.gemm_epilogue(c, s, 2.0, 0.0)
+    assert np.array_equal(two, 2.0 * one)
+    with_c, _ = oracle.gemm_epilogue(c, s, 1.0, 0.25, c_in)
+    assert np.allclose(with_c - one, 0.25 * c_in, rtol=0, atol=1e-12)
