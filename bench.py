@@ -6,6 +6,7 @@ A step is one call of the hot path on one batch of synthetic input:
   tiny / medium / compute   the other MXFP4 quant+GEMM shapes
   nvfp4_grouped     nvfp4_group_gemm over 8 groups (M_g 64..1024, N 4096, K 7168)
   mxfp4_grouped     mxfp4_group_gemm over the same groups with MXFP4 operands
+  nvfp4_decode      nvfp4_quant_gemm_fused on the decode shape (NVFP4 operands, fp16 C)
 Weights are pre-quantized once, untimed, by the library's own quantizer.
 
 Prints one JSON line (rank 0). `value` is microseconds per call over the whole
@@ -47,9 +48,10 @@ WORKLOADS = {
     "compute": wl.COMPUTE,
     "nvfp4_grouped": wl.NVFP4_GROUPED,
     "mxfp4_grouped": wl.MXFP4_GROUPED,
+    "nvfp4_decode": wl.NVFP4_DECODE,
 }
 DEFAULT_STEPS = {"decode": 20000, "tiny": 20000, "medium": 10000, "compute": 50, "nvfp4_grouped": 500,
-                 "mxfp4_grouped": 500}
+                 "mxfp4_grouped": 500, "nvfp4_decode": 20000}
 
 
 def grouped(name):
@@ -196,14 +198,17 @@ class ClockSampler:
 # ----------------------------------------------------------------- GPU arm --
 
 class MXCase:
-    """One MXFP4 quant+GEMM workload resident on the device, with L2 rotation."""
+    """One quant+GEMM workload resident on the device, with L2 rotation: MXFP4
+    (mxfp4_quant_gemm_fused), or NVFP4 (nvfp4_quant_gemm_fused) when w.vec == 16."""
 
     def __init__(self, w, dev, mx, torch):
         self.w, self.mx, self.torch = w, mx, torch
+        self.nv = w.vec == 16
         a_bits, b_bits = wl.gen_a(w), wl.gen_b(w)
         to = lambda bits: torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
         A0 = to(a_bits)
-        Bq0, Bsf0 = mx.mxfp4_quantize(to(b_bits))   # weight pre-quantization (untimed)
+        quant = mx.nvfp4_quantize if self.nv else mx.mxfp4_quantize
+        Bq0, Bsf0 = quant(to(b_bits))   # weight pre-quantization (untimed)
         torch.cuda.synchronize()
         self.a_host_bits = a_bits
         per = A0.numel() * 2 + Bq0.numel() + Bsf0.numel() + w.M * w.N * 2
@@ -212,17 +217,20 @@ class MXCase:
         self.A = [A0] + [A0.clone() for _ in range(self.rot - 1)]
         self.Bq = [Bq0.contiguous()] + [Bq0.contiguous().clone() for _ in range(self.rot - 1)]
         self.Bsf = [Bsf0] + [Bsf0.clone() for _ in range(self.rot - 1)]
-        self.C = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
+        self.C = torch.empty((w.M, w.N), dtype=torch.float16 if self.nv else torch.bfloat16, device=dev)
         self.ws = mx.new_workspace(w.M, w.N, w.K, dev)
         self.fused = w.M <= 64      # the library's fused small-M path (one launch)
         self.launches_per_step = 1 if self.fused else 2
-        plan = mx.gemm_plan(w.M, w.N, w.K, fused=True)
-        self.kernel_label, self.kernel_files = kernel_of(plan, "mxf4")
+        plan = mx.gemm_plan(w.M, w.N, w.K, fused=True, nvfp4=self.nv)
+        self.kernel_label, self.kernel_files = kernel_of(plan, "mxf4nvf4" if self.nv else "mxf4")
         self.rot_bytes = per * self.rot
 
     def step(self, i):
         j = i % self.rot
-        self.mx.mxfp4_quant_gemm_fused(self.A[j], self.Bq[j], self.Bsf[j], self.C, self.ws)
+        if self.nv:
+            self.mx.nvfp4_quant_gemm_fused(self.A[j], self.Bq[j], self.Bsf[j], self.C)
+        else:
+            self.mx.mxfp4_quant_gemm_fused(self.A[j], self.Bq[j], self.Bsf[j], self.C, self.ws)
 
     def prepare_gemm_only(self):
         """Pre-quantized A for timing the GEMM kernel of the two-kernel path alone."""
@@ -257,8 +265,9 @@ class MXCase:
         for _ in range(3):
             st = torch.cuda.Stream()
             A_dev = torch.empty_like(self.A[0])
-            C = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=A_dev.device)
-            c_pin = torch.empty((w.M, w.N), dtype=torch.bfloat16).pin_memory()
+            cdt = torch.float16 if self.nv else torch.bfloat16
+            C = torch.empty((w.M, w.N), dtype=cdt, device=A_dev.device)
+            c_pin = torch.empty((w.M, w.N), dtype=cdt).pin_memory()
             ws = mx.new_workspace(w.M, w.N, w.K, A_dev.device)
             sp = ctypes.c_void_p(st.cuda_stream)
             lanes.append((st, A_dev, C, c_pin, ws, sp))
@@ -271,11 +280,16 @@ class MXCase:
             else:
                 with torch.cuda.stream(st):
                     A_dev.copy_(a_pin, non_blocking=True)
-            status = L.mxfp4_quant_gemm_fused(A_dev.data_ptr(), A_dev.stride(0), self.Bq[j].data_ptr(),
-                                              self.Bq[j].stride(0), self.Bsf[j].data_ptr(), C.data_ptr(),
-                                              C.stride(0), w.M, w.N, w.K, ws.data_ptr(), ws.numel(), sp)
+            if self.nv:
+                status = L.nvfp4_quant_gemm_fused(A_dev.data_ptr(), A_dev.stride(0), self.Bq[j].data_ptr(),
+                                                  self.Bq[j].stride(0), self.Bsf[j].data_ptr(), C.data_ptr(),
+                                                  C.stride(0), w.M, w.N, w.K, sp)
+            else:
+                status = L.mxfp4_quant_gemm_fused(A_dev.data_ptr(), A_dev.stride(0), self.Bq[j].data_ptr(),
+                                                  self.Bq[j].stride(0), self.Bsf[j].data_ptr(), C.data_ptr(),
+                                                  C.stride(0), w.M, w.N, w.K, ws.data_ptr(), ws.numel(), sp)
             if status != 0:
-                raise RuntimeError(f"mxfp4_quant_gemm_fused returned {status}")
+                raise RuntimeError(f"quant+GEMM call returned {status}")
             if memcpy:
                 memcpy(c_pin.data_ptr(), C.data_ptr(), nC, 2, sp)
             else:
@@ -525,7 +539,7 @@ def _oracle_prep(name):
             prep.append((a_bits, qb, sfb))
     else:
         a_bits = wl.gen_a(w) if w.M <= 4096 else wl.gen_a(w, M=64)
-        qb, sfb = oracle.mx_quantize(wl.gen_b(w))
+        qb, sfb = (oracle.nv_quantize if w.vec == 16 else oracle.mx_quantize)(wl.gen_b(w))
         prep = (a_bits, qb, sfb)
     _ORACLE_PREP[name] = prep
     return prep
@@ -559,17 +573,18 @@ def oracle_call_sampled(name, budget_s):
         return (dt / done_rows * total_rows * 1e6,
                 f"first {r} rows of each group x all {w.N} columns (quantize + GEMM), scaled by rows")
     a_bits, qb, sfb = _oracle_prep(name)
+    quant = oracle.nv_quantize if w.vec == 16 else oracle.mx_quantize
     t0 = time.perf_counter()
-    qa, sfa = oracle.mx_quantize(a_bits[:1])
-    oracle.gemm_sampled(qa, sfa, qb, sfb, w.K, 32, np.zeros(w.N, np.int64), np.arange(w.N))
+    qa, sfa = quant(a_bits[:1])
+    oracle.gemm_sampled(qa, sfa, qb, sfb, w.K, w.vec, np.zeros(w.N, np.int64), np.arange(w.N))
     per_row = time.perf_counter() - t0
     r = max(1, min(w.M, a_bits.shape[0], int(budget_s / per_row)))
     t0 = time.perf_counter()
-    qa, sfa = oracle.mx_quantize(a_bits[:r])
+    qa, sfa = quant(a_bits[:r])
     if r == w.M:
-        oracle.gemm_full(qa, sfa, qb, sfb, w.K, 32)
+        oracle.gemm_full(qa, sfa, qb, sfb, w.K, w.vec)
     else:
-        oracle.gemm_sampled(qa, sfa, qb, sfb, w.K, 32, np.repeat(np.arange(r), w.N), np.tile(np.arange(w.N), r))
+        oracle.gemm_sampled(qa, sfa, qb, sfb, w.K, w.vec, np.repeat(np.arange(r), w.N), np.tile(np.arange(w.N), r))
     dt = time.perf_counter() - t0
     full = "the full call" if r == w.M else f"rows 0..{r - 1} of {w.M} x all {w.N} columns, scaled by rows"
     return dt / r * w.M * 1e6, f"{full} (quantize A + dequantize-then-fp64 GEMM)"

@@ -514,8 +514,8 @@ mxfp4_status_t mxfp4_quant_gemm_fused(const void *A, int64_t lda, const void *Bq
         CUtensorMap tmw;
         st = fp4_map(Bq, K / 2, N, ldbq, 128, &tmw);
         if (st != MXFP4_OK) return st;
-        return cuda_status(launch_fused_mx(tmw, A, lda, static_cast<const uint8_t *>(B_sf), C, ldc,
-                                           static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), fp, s));
+        return cuda_status(launch_fused(tmw, A, lda, static_cast<const uint8_t *>(B_sf), C, ldc,
+                                        static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), fp, false, s));
     }
     // two-kernel path: quantize A into the workspace, then the GEMM
     uint8_t *w = static_cast<uint8_t *>(workspace);
@@ -524,6 +524,28 @@ mxfp4_status_t mxfp4_quant_gemm_fused(const void *A, int64_t lda, const void *Bq
     st = cuda_status(launch_quant_mx(A, M, K, lda, aq, wl.ldq, asf, sms, s));
     if (st != MXFP4_OK) return st;
     return run_gemm(aq, wl.ldq, asf, Bq, ldbq, B_sf, C, ldc, M, N, K, workspace, wl, s);
+}
+
+mxfp4_status_t nvfp4_quant_gemm_fused(const void *A, int64_t lda, const void *Bq, int64_t ldbq, const void *B_sf,
+                                      void *C, int64_t ldc, int64_t M, int64_t N, int64_t K, void *stream)
+{
+    if (!A || !Bq || !B_sf || !C) return MXFP4_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 1 || N > kMaxDim || K > kMaxDim) return MXFP4_ERR_INVALID_ARG;
+    if (K % 16 != 0 || M > 64) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+    if (lda < K || ldbq < K / 2 || ldc < N) return MXFP4_ERR_INVALID_ARG;
+    if ((lda * 2) % 16 != 0 || ldbq % 16 != 0) return MXFP4_ERR_MISALIGNED;
+    if (!al16(A) || !al16(Bq) || !al16(B_sf) || !al2(C)) return MXFP4_ERR_MISALIGNED;
+    int sms = 0;
+    mxfp4_status_t st = current_device(&sms);
+    if (st != MXFP4_OK) return st;
+    FusedPlan fp;
+    if (!plan_fused(M, N, K, sms, &fp, true)) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+    CUtensorMap tmw;
+    st = fp4_map(Bq, K / 2, N, ldbq, 128, &tmw);
+    if (st != MXFP4_OK) return st;
+    return cuda_status(launch_fused(tmw, A, lda, static_cast<const uint8_t *>(B_sf), C, ldc, static_cast<int>(M),
+                                    static_cast<int>(N), static_cast<int>(K), fp, true,
+                                    static_cast<cudaStream_t>(stream)));
 }
 
 mxfp4_status_t nvfp4_group_gemm(const nvfp4_problem_t *problems, int num_groups, void *workspace, size_t ws_bytes,
@@ -541,15 +563,15 @@ mxfp4_status_t mxfp4_group_gemm(const mxfp4_problem_t *problems, int num_groups,
 
 mxfp4_status_t mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, int which, mxfp4_plan_t *out)
 {
-    if (!out || (which != 0 && which != 1)) return MXFP4_ERR_INVALID_ARG;
+    if (!out || which < 0 || which > 2) return MXFP4_ERR_INVALID_ARG;
     if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return MXFP4_ERR_INVALID_ARG;
-    if (K % 32 != 0) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+    if (K % (which == 2 ? 16 : 32) != 0 || (which == 2 && M > 64)) return MXFP4_ERR_UNSUPPORTED_SHAPE;
     int sms = 0;
     const mxfp4_status_t st = current_device(&sms);
     if (st != MXFP4_OK) return st;
     memset(out, 0, sizeof(*out));
     FusedPlan fp;
-    if (which == 1 && plan_fused(M, N, K, sms, &fp)) {
+    if (which >= 1 && plan_fused(M, N, K, sms, &fp, which == 2)) {
         out->kernel = MXFP4_KERNEL_FUSED;
         out->tile_m = fp.mma_n;   // activation rows (padded) x 128 weight rows
         out->tile_n = 128;

@@ -43,7 +43,10 @@ namespace {
 
 constexpr int kRing = 4;
 constexpr uint32_t kWBytes = 128 * 128;   // one stage of 128 weight rows x 256 FP4
-constexpr uint32_t kWSfBytes = 2 * 512;   // its two 512-byte scale blocks
+// NV selects NVFP4 (E4M3 scale per 16, kind::mxf4nvf4, fp16 C); otherwise
+// MXFP4 (E8M0 per 32, kind::mxf4, bf16 C).
+template <bool NV>
+constexpr int kSfBlk = NV ? 4 : 2;         // 512-byte scale blocks per 128 rows per stage
 constexpr int kThreads = 192;
 constexpr int kStageWarps = 4;           // warps 2-5: quantize + issue MMAs
 constexpr int kMaxSplits = 8;             // portable cluster size
@@ -54,23 +57,26 @@ __host__ __device__ constexpr uint32_t pow2_cols_f(uint32_t n)
     return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : n <= 256 ? 256 : 512;
 }
 
-template <int MMA_N>
+template <int MMA_N, bool NV = false>
 struct FusedCfg {
+    static constexpr int SF_BLK = kSfBlk<NV>;
+    static constexpr uint32_t SF_STAGE = SF_BLK * 512;     // one operand's scale bytes per stage
     // K stages (256 wide) held per CTA: each has its own quantized operand tile
-    // and its own TMEM scale columns.
-    static constexpr int MAX_ST = MMA_N <= 16 ? 8 : 4;
+    // and its own TMEM scale columns (fewer with NVFP4's larger scale blocks,
+    // so that two CTAs still share an SM).
+    static constexpr int MAX_ST = MMA_N <= 16 ? (NV ? 6 : 8) : 4;
     static constexpr int BPL = MMA_N * 8 / 32;              // 32-blocks per lane per stage
     static constexpr uint32_t ACT_TILE = MMA_N * 128;       // quantized operand bytes per stage
     static constexpr uint32_t RING_DATA = kRing * kWBytes;
     static constexpr uint32_t ACT_OFF = RING_DATA;
     static constexpr uint32_t WSF_OFF = ACT_OFF + MAX_ST * ACT_TILE;
-    static constexpr uint32_t ASF_OFF = WSF_OFF + kRing * kWSfBytes;
-    static constexpr uint32_t RECV_OFF = ASF_OFF + MAX_ST * 1024;
+    static constexpr uint32_t ASF_OFF = WSF_OFF + kRing * SF_STAGE;
+    static constexpr uint32_t RECV_OFF = ASF_OFF + MAX_ST * SF_STAGE;
     // [source rank][m][owned rows] fp32; owned rows = ceil(128 / S) <= 128 / S + 1
     static constexpr uint32_t RECV_BYTES = MMA_N * (128 + kMaxSplits) * 4;
     static constexpr uint32_t BAR_OFF = RECV_OFF + RECV_BYTES;
     static constexpr uint32_t SMEM_BYTES = BAR_OFF + 256 + 1024;
-    static constexpr uint32_t SF_COLS = 16;                  // per stage: 8 weight + 8 activation
+    static constexpr uint32_t SF_COLS = 2 * SF_BLK * 4;      // per stage: weight + activation blocks
     static constexpr uint32_t ACC_COLS = kStageWarps * MMA_N;  // one accumulator per stage warp
     static constexpr uint32_t TMEM_COLS = pow2_cols_f(ACC_COLS + MAX_ST * SF_COLS);
     static_assert(BPL % kBatch == 0, "quant work split");
@@ -83,25 +89,35 @@ struct FusedCfg {
 struct FusedArgs {
     const uint16_t *A;    // bf16 [M, K], row stride lda elements
     int64_t lda;
-    const uint8_t *sfw;   // weight scales, blocked [N, K/32]
-    __nv_bfloat16 *C;
+    const uint8_t *sfw;   // weight scales, blocked [N, K/32] (MXFP4) or [N, K/16] (NVFP4)
+    uint16_t *C;          // bf16 (MXFP4) or fp16 (NVFP4) [M, N]
     int64_t ldc;
     int M, N, K;
     int splits;
     int sf_cblocks;
 };
 
-template <int MMA_N>
+// C element from fp32: bf16 (MXFP4) or fp16 (NVFP4), round to nearest even.
+template <bool NV>
+__device__ __forceinline__ uint16_t to_c(float f)
+{
+    if constexpr (NV)
+        return __half_as_ushort(__float2half_rn(f));
+    else
+        return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+template <int MMA_N, bool NV>
 __global__ void __launch_bounds__(kThreads, 2)
     fused_quant_gemm_kernel(const __grid_constant__ CUtensorMap tmw, const FusedArgs p)
 {
-    using Cfg = FusedCfg<MMA_N>;
+    using Cfg = FusedCfg<MMA_N, NV>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *ring = smem;
     uint8_t *act = smem + Cfg::ACT_OFF;       // [stage][MMA_N rows x 128 B], 128B-swizzled
-    uint8_t *ring_sf = smem + Cfg::WSF_OFF;   // [slot][2 x 512 B]
-    uint8_t *act_sf = smem + Cfg::ASF_OFF;    // [stage][2 x 512 B]
+    uint8_t *ring_sf = smem + Cfg::WSF_OFF;   // [slot][SF_BLK x 512 B]
+    uint8_t *act_sf = smem + Cfg::ASF_OFF;    // [stage][SF_BLK x 512 B]
     float *recv = reinterpret_cast<float *>(smem + Cfg::RECV_OFF);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::BAR_OFF);
     uint64_t *empty = full + kRing;
@@ -124,11 +140,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     auto issue_weights = [&](int i) {
         const int slot = i % kRing;
         const int ks = s_begin + i;
-        const int blk0 = ks * 2;
-        const int nblk = min(2, p.sf_cblocks - blk0);
+        const int blk0 = ks * Cfg::SF_BLK;
+        const int nblk = min(Cfg::SF_BLK, p.sf_cblocks - blk0);
         mbar_arrive_expect_tx(full + slot, kWBytes + nblk * 512);
         tma_load_2d(ring + slot * kWBytes, &tmw, ks * 128, n_tile * 128, full + slot, pol_w);
-        bulk_load(ring_sf + slot * kWSfBytes, p.sfw + (static_cast<size_t>(n_tile) * p.sf_cblocks + blk0) * 512,
+        bulk_load(ring_sf + slot * Cfg::SF_STAGE, p.sfw + (static_cast<size_t>(n_tile) * p.sf_cblocks + blk0) * 512,
                   nblk * 512, full + slot, pol_w);
         issued = i + 1;
     };
@@ -190,12 +206,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         // and blocks past K are zero and quantize to code 0 with scale byte 0.
         const int sw = warp - 2;
         const uint32_t acc_tmem = tmem + static_cast<uint32_t>(sw * MMA_N);
-        constexpr uint32_t IDESC = idesc_block_scaled(MMA_N, true);
+        constexpr uint32_t IDESC = idesc_block_scaled(MMA_N, !NV);
         bool first = true;
         for (int t = sw; t < nst; t += kStageWarps) {
             const int ks = s_begin + t;
             uint8_t *dst = act + t * Cfg::ACT_TILE;
-            uint8_t *dsf = act_sf + t * 1024;
+            uint8_t *dsf = act_sf + t * Cfg::SF_STAGE;
 #pragma unroll 1
             for (int e0 = 0; e0 < Cfg::BPL; e0 += kBatch) {
                 uint4 v[kBatch][4];
@@ -213,16 +229,38 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int x = 0; x < kBatch; ++x) {
                     const int u = lane + 32 * (e0 + x);
                     const int m = u >> 3, j = u & 7;
-                    const uint32_t pair = umax16x2(umax16x2(max_abs_pair8(v[x][0]), max_abs_pair8(v[x][1])),
-                                                   umax16x2(max_abs_pair8(v[x][2]), max_abs_pair8(v[x][3])));
-                    const uint32_t sbyte = e8m0_byte_from_amax(max(pair & 0xFFFFu, pair >> 16));
                     uint4 codes;
-                    codes.x = mx_codes8(v[x][0], sbyte);
-                    codes.y = mx_codes8(v[x][1], sbyte);
-                    codes.z = mx_codes8(v[x][2], sbyte);
-                    codes.w = mx_codes8(v[x][3], sbyte);
+                    if constexpr (NV) {
+                        // two 16-element groups, each with s = E4M3(fp32(amax) / 6)
+                        // and codes of x / s, as the standalone NVFP4 quantizer
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint32_t pr = umax16x2(max_abs_pair8(v[x][2 * h]), max_abs_pair8(v[x][2 * h + 1]));
+                            const uint32_t amax = max(pr & 0xFFFFu, pr >> 16);
+                            const uint32_t sbyte = e4m3_rn_sat(__fdiv_rn(__uint_as_float(amax << 16), 6.0f));
+                            const float sv = e4m3_value(sbyte);
+                            const uint32_t lo = nv_codes8(v[x][2 * h], sv), hi = nv_codes8(v[x][2 * h + 1], sv);
+                            if (h == 0) {
+                                codes.x = lo;
+                                codes.y = hi;
+                            } else {
+                                codes.z = lo;
+                                codes.w = hi;
+                            }
+                            const int c = 2 * j + h;   // scale column within the stage (16 per stage)
+                            dsf[(c >> 2) * 512 + (m & 31) * 16 + (m >> 5) * 4 + (c & 3)] = static_cast<uint8_t>(sbyte);
+                        }
+                    } else {
+                        const uint32_t pair = umax16x2(umax16x2(max_abs_pair8(v[x][0]), max_abs_pair8(v[x][1])),
+                                                       umax16x2(max_abs_pair8(v[x][2]), max_abs_pair8(v[x][3])));
+                        const uint32_t sbyte = e8m0_byte_from_amax(max(pair & 0xFFFFu, pair >> 16));
+                        codes.x = mx_codes8(v[x][0], sbyte);
+                        codes.y = mx_codes8(v[x][1], sbyte);
+                        codes.z = mx_codes8(v[x][2], sbyte);
+                        codes.w = mx_codes8(v[x][3], sbyte);
+                        dsf[(j >> 2) * 512 + (m & 31) * 16 + (m >> 5) * 4 + (j & 3)] = static_cast<uint8_t>(sbyte);
+                    }
                     *reinterpret_cast<uint4 *>(dst + m * 128 + ((j ^ (m & 7)) << 4)) = codes;
-                    dsf[(j >> 2) * 512 + (m & 31) * 16 + (m >> 5) * 4 + (j & 3)] = static_cast<uint8_t>(sbyte);
                 }
             }
             fence_proxy_async_smem();   // generic-proxy writes -> visible to tcgen05
@@ -235,22 +273,27 @@ __global__ void __launch_bounds__(kThreads, 2)
                     tc_fence_after();
                     const uint32_t w_base = smem_u32(ring + slot * kWBytes);
                     const uint32_t a_base = smem_u32(dst);
-                    const uint32_t wsf = smem_u32(ring_sf + slot * kWSfBytes);
+                    const uint32_t wsf = smem_u32(ring_sf + slot * Cfg::SF_STAGE);
                     const uint32_t asf = smem_u32(dsf);
                     const uint32_t tsfw = tmem + Cfg::ACC_COLS + t * Cfg::SF_COLS;
-                    const uint32_t tsfa = tsfw + 8;
+                    const uint32_t tsfa = tsfw + Cfg::SF_BLK * 4;
                     const int ksteps = min(4, k_steps_total - ks * 4);
-                    const int nblk = (ksteps + 1) / 2;
+                    const int nblk = NV ? ksteps : (ksteps + 1) / 2;
                     for (int b = 0; b < nblk; ++b) {
                         tc_cp_scale_block(tsfw + b * 4, sdesc_scale(wsf + b * 512));
                         tc_cp_scale_block(tsfa + b * 4, sdesc_scale(asf + b * 512));
                     }
                     for (int kk = 0; kk < ksteps; ++kk) {
-                        const uint32_t sfid = static_cast<uint32_t>(kk & 1) * 2u;
-                        const int blk = kk >> 1;
-                        mma_mxf4(acc_tmem, sdesc_sw128(w_base + kk * 32), sdesc_sw128(a_base + kk * 32),
-                                 idesc_with_sf_ids(IDESC, sfid, sfid), tsfw + blk * 4, tsfa + blk * 4,
-                                 (first && kk == 0) ? 0u : 1u);
+                        const uint32_t sfid = NV ? 0u : static_cast<uint32_t>(kk & 1) * 2u;
+                        const int blk = NV ? kk : kk >> 1;
+                        const uint32_t idesc = idesc_with_sf_ids(IDESC, sfid, sfid);
+                        const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+                        if constexpr (NV)
+                            mma_nvf4(acc_tmem, sdesc_sw128(w_base + kk * 32), sdesc_sw128(a_base + kk * 32), idesc,
+                                     tsfw + blk * 4, tsfa + blk * 4, acc);
+                        else
+                            mma_mxf4(acc_tmem, sdesc_sw128(w_base + kk * 32), sdesc_sw128(a_base + kk * 32), idesc,
+                                     tsfw + blk * 4, tsfa + blk * 4, acc);
                     }
                     tc_commit(empty + slot);
                 }
@@ -307,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int m = c0 + j;
-                    if (m < p.M && n < p.N) p.C[static_cast<int64_t>(m) * p.ldc + n] = __float2bfloat16_rn(f[j]);
+                    if (m < p.M && n < p.N) p.C[static_cast<int64_t>(m) * p.ldc + n] = to_c<NV>(f[j]);
                 }
             } else {
 #pragma unroll
@@ -332,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (n >= p.N) continue;
                 float s = 0.0f;
                 for (int r = 0; r < S; ++r) s += recv[(r * MMA_N + m) * nper + nl];
-                p.C[static_cast<int64_t>(m) * p.ldc + n] = __float2bfloat16_rn(s);
+                p.C[static_cast<int64_t>(m) * p.ldc + n] = to_c<NV>(s);
             }
         }
     }
@@ -351,12 +394,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
-template <int MMA_N>
+template <int MMA_N, bool NV>
 cudaError_t launch_fused_t(const CUtensorMap &tmw, const FusedArgs &args, int n_tiles, int splits,
                            cudaStream_t stream)
 {
-    using Cfg = FusedCfg<MMA_N>;
-    auto kern = fused_quant_gemm_kernel<MMA_N>;
+    using Cfg = FusedCfg<MMA_N, NV>;
+    auto kern = fused_quant_gemm_kernel<MMA_N, NV>;
     static uint64_t configured = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -386,11 +429,14 @@ cudaError_t launch_fused_t(const CUtensorMap &tmw, const FusedArgs &args, int n_
 
 }  // namespace
 
-bool plan_fused(int64_t M, int64_t N, int64_t K, int num_sms, FusedPlan *plan)
+bool plan_fused(int64_t M, int64_t N, int64_t K, int num_sms, FusedPlan *plan, bool nvfp4)
 {
-    if (M < 1 || M > 64 || N < 1 || K < 32) return false;
+    if (M < 1 || M > 64 || N < 1 || K < (nvfp4 ? 16 : 32)) return false;
     const int mma_n = M <= 16 ? 16 : M <= 32 ? 32 : 64;
-    const int max_st = mma_n == 16 ? FusedCfg<16>::MAX_ST : mma_n == 32 ? FusedCfg<32>::MAX_ST : FusedCfg<64>::MAX_ST;
+    const int max_st = nvfp4 ? (mma_n == 16 ? FusedCfg<16, true>::MAX_ST
+                                            : mma_n == 32 ? FusedCfg<32, true>::MAX_ST : FusedCfg<64, true>::MAX_ST)
+                             : (mma_n == 16 ? FusedCfg<16>::MAX_ST
+                                            : mma_n == 32 ? FusedCfg<32>::MAX_ST : FusedCfg<64>::MAX_ST);
     const int64_t k_stages = (K + 255) / 256;
     const int64_t n_tiles = (N + 127) / 128;
     int64_t s = (num_sms + n_tiles / 2) / n_tiles;
@@ -406,24 +452,32 @@ bool plan_fused(int64_t M, int64_t N, int64_t K, int num_sms, FusedPlan *plan)
     return true;
 }
 
-cudaError_t launch_fused_mx(const CUtensorMap &tmb, const void *A, int64_t lda, const uint8_t *sfb, void *C,
-                            int64_t ldc, int M, int N, int K, const FusedPlan &plan, cudaStream_t stream)
+cudaError_t launch_fused(const CUtensorMap &tmb, const void *A, int64_t lda, const uint8_t *sfb, void *C,
+                         int64_t ldc, int M, int N, int K, const FusedPlan &plan, bool nvfp4, cudaStream_t stream)
 {
     FusedArgs a;
     a.A = static_cast<const uint16_t *>(A);
     a.lda = lda;
     a.sfw = sfb;
-    a.C = static_cast<__nv_bfloat16 *>(C);
+    a.C = static_cast<uint16_t *>(C);
     a.ldc = ldc;
     a.M = M;
     a.N = N;
     a.K = K;
     a.splits = plan.splits;
-    a.sf_cblocks = (K / 32 + 3) / 4;
+    a.sf_cblocks = (K / (nvfp4 ? 16 : 32) + 3) / 4;
+    if (nvfp4) {
+        switch (plan.mma_n) {
+        case 16: return launch_fused_t<16, true>(tmb, a, plan.n_tiles, plan.splits, stream);
+        case 32: return launch_fused_t<32, true>(tmb, a, plan.n_tiles, plan.splits, stream);
+        case 64: return launch_fused_t<64, true>(tmb, a, plan.n_tiles, plan.splits, stream);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     switch (plan.mma_n) {
-    case 16: return launch_fused_t<16>(tmb, a, plan.n_tiles, plan.splits, stream);
-    case 32: return launch_fused_t<32>(tmb, a, plan.n_tiles, plan.splits, stream);
-    case 64: return launch_fused_t<64>(tmb, a, plan.n_tiles, plan.splits, stream);
+    case 16: return launch_fused_t<16, false>(tmb, a, plan.n_tiles, plan.splits, stream);
+    case 32: return launch_fused_t<32, false>(tmb, a, plan.n_tiles, plan.splits, stream);
+    case 64: return launch_fused_t<64, false>(tmb, a, plan.n_tiles, plan.splits, stream);
     default: return cudaErrorInvalidValue;
     }
 }

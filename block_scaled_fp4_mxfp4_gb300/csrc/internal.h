@@ -73,11 +73,12 @@ struct FusedPlan {
     int n_tiles;     // ceil(N / 128)
 };
 // Whether the fused small-M kernel can run (M, K) and with which plan.
-bool plan_fused(int64_t M, int64_t N, int64_t K, int num_sms, FusedPlan *plan);
+// nvfp4: E4M3 scales per 16 and fp16 C (else MXFP4: E8M0 per 32, bf16 C).
+bool plan_fused(int64_t M, int64_t N, int64_t K, int num_sms, FusedPlan *plan, bool nvfp4 = false);
 // tmb: packed weights [N, K/2], box {128 B, 128 rows}, 128B swizzle.
-cudaError_t launch_fused_mx(const CUtensorMap &tmb, const void *A, int64_t lda, const uint8_t *sfb,
-                            void *C, int64_t ldc, int M, int N, int K, const FusedPlan &plan,
-                            cudaStream_t stream);
+cudaError_t launch_fused(const CUtensorMap &tmb, const void *A, int64_t lda, const uint8_t *sfb,
+                         void *C, int64_t ldc, int M, int N, int K, const FusedPlan &plan, bool nvfp4,
+                         cudaStream_t stream);
 int read_and_clear_fused_error();
 
 }  // namespace mxfp4

@@ -83,6 +83,8 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
                                      ctypes.c_float, ctypes.c_float, _p, _p, _sz, _p]
     L.mxfp4_quant_gemm_fused.restype = _st
     L.mxfp4_quant_gemm_fused.argtypes = [_p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p, _sz, _p]
+    L.nvfp4_quant_gemm_fused.restype = _st
+    L.nvfp4_quant_gemm_fused.argtypes = [_p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p]
     L.nvfp4_group_gemm.restype = _st
     L.nvfp4_group_gemm.argtypes = [ctypes.POINTER(NvProblem), ctypes.c_int, _p, _sz, _p]
     L.mxfp4_noalloc_scratch_bytes.restype = _sz
@@ -258,6 +260,21 @@ def mxfp4_quant_gemm_fused(A, Bq, B_sf, C=None, workspace=None, stream=None):
     return C
 
 
+def nvfp4_quant_gemm_fused(A, Bq, B_sf, C=None, stream=None):
+    """C [M, N] fp16 = NVFP4(A) x (Bq, B_sf)^T for M <= 64, quantization fused into the GEMM."""
+    _dev(A, "A", torch.bfloat16, 2)
+    _dev(Bq, "Bq", torch.uint8, 2)
+    M, K = A.shape
+    N = Bq.shape[0]
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float16, device=A.device)
+    _dev(C, "C", torch.float16, 2)
+    _check(_lib.nvfp4_quant_gemm_fused(A.data_ptr(), A.stride(0), Bq.data_ptr(), Bq.stride(0), B_sf.data_ptr(),
+                                       C.data_ptr(), C.stride(0), M, N, K, _stream_ptr(stream)),
+           "nvfp4_quant_gemm_fused")
+    return C
+
+
 def make_nv_problems(groups, struct=None):
     """ctypes array of nvfp4_problem_t (or `struct`) from dicts with keys a, sfa,
     b, sfb, c, k."""
@@ -307,11 +324,13 @@ def _plan_dict(p: Plan) -> dict:
                 splits=p.splits, tiles=p.tiles, quant_launch=bool(p.quant_launch))
 
 
-def gemm_plan(M: int, N: int, K: int, fused: bool = False) -> dict:
-    """What mxfp4_gemm_a4w4 (fused=False) or mxfp4_quant_gemm_fused (fused=True)
-    launches for an M x N x K problem on the current device."""
+def gemm_plan(M: int, N: int, K: int, fused: bool = False, nvfp4: bool = False) -> dict:
+    """What mxfp4_gemm_a4w4 (fused=False), mxfp4_quant_gemm_fused (fused=True) or
+    nvfp4_quant_gemm_fused (nvfp4=True) launches for an M x N x K problem on the
+    current device."""
     p = Plan()
-    _check(lib().mxfp4_gemm_plan(M, N, K, 1 if fused else 0, ctypes.byref(p)), "mxfp4_gemm_plan")
+    which = 2 if nvfp4 else (1 if fused else 0)
+    _check(lib().mxfp4_gemm_plan(M, N, K, which, ctypes.byref(p)), "mxfp4_gemm_plan")
     return _plan_dict(p)
 
 

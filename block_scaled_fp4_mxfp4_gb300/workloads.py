@@ -80,7 +80,8 @@ def bf16_bits_to_float(bits: np.ndarray) -> np.ndarray:
 
 @dataclass
 class MXWorkload:
-    """MXFP4 quant+GEMM problem: bf16 A [M, K] (dynamic), bf16 B [N, K] (pre-quantized)."""
+    """Quant+GEMM problem: bf16 A [M, K] (dynamic), bf16 B [N, K] (pre-quantized);
+    MXFP4 (E8M0 per 32, bf16 C), or NVFP4 (E4M3 per 16, fp16 C) when vec == 16."""
     name: str
     M: int
     N: int
@@ -89,6 +90,7 @@ class MXWorkload:
     a_sigma: float = 1.0
     b_sigma: float = 1.0
     seed: int = 0
+    vec: int = 32
 
     @property
     def flops(self) -> int:
@@ -96,8 +98,8 @@ class MXWorkload:
 
     @property
     def alg_bytes(self) -> int:
-        """bf16 A + packed B + B's E8M0 scales + bf16 C (quantized A is not counted)."""
-        return 2 * self.M * self.K + self.N * self.K // 2 + self.N * self.K // 32 + 2 * self.M * self.N
+        """bf16 A + packed B + B's scales + 16-bit C (quantized A is not counted)."""
+        return 2 * self.M * self.K + self.N * self.K // 2 + self.N * self.K // self.vec + 2 * self.M * self.N
 
 
 @dataclass
@@ -134,6 +136,10 @@ NVFP4_GROUPED = NVWorkload("nvfp4_grouped_8x_N4096_K7168",
 # MXFP4 (mixture-of-experts) GEMM beyond the pages' single-problem MXFP4 call.
 MXFP4_GROUPED = NVWorkload("mxfp4_grouped_8x_N4096_K7168",
                            [64, 128, 256, 384, 512, 640, 768, 1024], 4096, 7168, vec=32)
+
+# The decode shape with NVFP4 operands: the fused NVFP4 quant + GEMM (the NVFP4
+# twin of the fused MXFP4 path).
+NVFP4_DECODE = MXWorkload("nvfp4_decode_M16_N2112_K7168", 16, 2112, 7168, "normal", 1.0, 0.02, vec=16)
 
 MX_WORKLOADS = {w.name: w for w in (TINY, DECODE, MEDIUM, COMPUTE)}
 

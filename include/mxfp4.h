@@ -171,6 +171,20 @@ MXFP4_API mxfp4_status_t mxfp4_quant_gemm_fused(const void *A, int64_t lda, cons
                                       int64_t N, int64_t K, void *workspace, size_t ws_bytes,
                                       void *stream);
 
+/* The NVFP4 twin of mxfp4_quant_gemm_fused for small M (1 <= M <= 64):
+ * dynamic NVFP4 quantization of bf16 A (per 16 elements along K: scale
+ * s = E4M3_RNE_sat(fp32(amax) / 6), codes E2M1_RNE_sat(fp32(x) / s), as
+ * nvfp4_quantize) fused on chip with the block-scaled GEMM against a
+ * pre-quantized NVFP4 B (E2M1 [N, K/2], blocked E4M3 scales
+ * mxfp4_sf_bytes(N, K, 16)):
+ *   C[m, n] = fp16_rne( sum_k A_q[m, k] * B_q[n, k] )   (fp32 accumulation)
+ * The quantized A never reaches global memory; no workspace. K % 16 == 0;
+ * M > 64 returns MXFP4_ERR_UNSUPPORTED_SHAPE (use nvfp4_quantize and
+ * nvfp4_group_gemm there). Alignment as for mxfp4_quant_gemm_fused. */
+MXFP4_API mxfp4_status_t nvfp4_quant_gemm_fused(const void *A, int64_t lda, const void *Bq, int64_t ldbq,
+                                                const void *B_sf, void *C, int64_t ldc, int64_t M, int64_t N,
+                                                int64_t K, void *stream);
+
 /* One problem of a grouped NVFP4 GEMM ([NV-496271] custom_kernel: each entry of
  * the problem list carries a, b, c, their scales and (m, n, k)). */
 typedef struct {
@@ -272,8 +286,9 @@ typedef struct {
     int quant_launch;
 } mxfp4_plan_t;
 
-/* The plan of mxfp4_gemm_a4w4 (which = 0) or mxfp4_quant_gemm_fused
- * (which = 1) for an M x N x K problem on the current device. Launches
+/* The plan of mxfp4_gemm_a4w4 (which = 0), mxfp4_quant_gemm_fused
+ * (which = 1) or nvfp4_quant_gemm_fused (which = 2) for an M x N x K problem
+ * on the current device. Launches
  * nothing; reads the device's SM count (MXFP4_ERR_NO_DEVICE without a usable
  * GB300). Argument checks as for the calls themselves, minus the pointers. */
 MXFP4_API mxfp4_status_t mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, int which, mxfp4_plan_t *out);

@@ -14,7 +14,7 @@ L = mxfp4.lib()
 
 def test_every_declared_symbol_is_exported():
     names = mxfp4.declared_symbols()
-    assert len(names) == 18
+    assert len(names) == 19
     for n in names:
         assert hasattr(L, n), n  # ctypes resolves the exported symbol
 
@@ -105,7 +105,9 @@ def test_valid_call_without_gpu_reports_no_device():
 def test_plan_argument_validation_needs_no_gpu():
     plan = mxfp4.Plan()
     assert L.mxfp4_gemm_plan(16, 2112, 7168, 1, None) == 1          # no output struct
-    assert L.mxfp4_gemm_plan(16, 2112, 7168, 2, ctypes.byref(plan)) == 1   # which must be 0 or 1
+    assert L.mxfp4_gemm_plan(16, 2112, 7168, 3, ctypes.byref(plan)) == 1   # which must be 0, 1 or 2
+    assert L.mxfp4_gemm_plan(65, 2112, 7168, 2, ctypes.byref(plan)) == 2  # fused NVFP4: M <= 64
+    assert L.mxfp4_gemm_plan(16, 2112, 7176, 2, ctypes.byref(plan)) == 2  # K % 32 for the fused path too
     assert L.mxfp4_gemm_plan(0, 2112, 7168, 0, ctypes.byref(plan)) == 1
     assert L.mxfp4_gemm_plan(16, 2112, 7000, 0, ctypes.byref(plan)) == 2   # K % 32
     probs = (mxfp4.NvProblem * 1)()
@@ -152,3 +154,11 @@ def test_gemm_ex_argument_validation_needs_no_gpu():
     assert call(bias=17) == 3          # bias must be 2-byte aligned
     assert call(K=1000) == 2           # K % 32
     assert call(ws=0) == 1
+
+
+def test_nvfp4_fused_argument_validation_needs_no_gpu():
+    f = L.nvfp4_quant_gemm_fused
+    assert f(16, 1024, 16, 512, 16, 16, 64, 65, 64, 1024, None) == 2     # M > 64
+    assert f(16, 1024, 16, 512, 16, 16, 64, 8, 64, 1000, None) == 2      # K % 16
+    assert f(None, 1024, 16, 512, 16, 16, 64, 8, 64, 1024, None) == 1
+    assert f(16, 1028, 16, 512, 16, 16, 64, 8, 64, 1024, None) == 3      # lda * 2 % 16
