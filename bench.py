@@ -7,6 +7,8 @@ A step is one call of the hot path on one batch of synthetic input:
   nvfp4_grouped     nvfp4_group_gemm over 8 groups (M_g 64..1024, N 4096, K 7168)
   mxfp4_grouped     mxfp4_group_gemm over the same groups with MXFP4 operands
   nvfp4_decode      nvfp4_quant_gemm_fused on the decode shape (NVFP4 operands, fp16 C)
+  nvfp4_grouped_bf16  nvfp4_group_quant_gemm: the nvfp4_grouped shapes with bf16 A_g,
+                    quantized inside every call (grouped quantization + grouped GEMM)
 Weights are pre-quantized once, untimed, by the library's own quantizer.
 
 Prints one JSON line (rank 0). `value` is microseconds per call over the whole
@@ -49,9 +51,10 @@ WORKLOADS = {
     "nvfp4_grouped": wl.NVFP4_GROUPED,
     "mxfp4_grouped": wl.MXFP4_GROUPED,
     "nvfp4_decode": wl.NVFP4_DECODE,
+    "nvfp4_grouped_bf16": wl.NVFP4_GROUPED_BF16,
 }
 DEFAULT_STEPS = {"decode": 20000, "tiny": 20000, "medium": 10000, "compute": 50, "nvfp4_grouped": 500,
-                 "mxfp4_grouped": 500, "nvfp4_decode": 20000}
+                 "mxfp4_grouped": 500, "nvfp4_decode": 20000, "nvfp4_grouped_bf16": 500}
 
 
 def grouped(name):
@@ -334,20 +337,25 @@ def _cuda_memcpy_async():
 
 class NVCase:
     """Grouped workload (NVFP4, or MXFP4 when w.vec == 32): operands quantized
-    once (untimed) by nvfp4_quantize / mxfp4_quantize."""
+    once (untimed) by nvfp4_quantize / mxfp4_quantize; with w.bf16_a the A_g stay
+    bf16 and nvfp4_group_quant_gemm quantizes them inside every call."""
 
     def __init__(self, w, dev, mx, torch):
         self.w, self.mx, self.torch = w, mx, torch
         nv = w.vec == 16
         quant = mx.nvfp4_quantize if nv else mx.mxfp4_quantize
         to = lambda bits: torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
-        self.groups = []
+        self.groups = []     # pre-quantized operands (the grouped GEMM's own inputs)
+        self.act = []        # bf16 activations (w.bf16_a)
         for g in range(len(w.Ms)):
             a_bits, b_bits = wl.gen_nv_group(w, g)
-            qa, sfa = quant(to(a_bits))
+            a16 = to(a_bits)
+            qa, sfa = quant(a16)
             qb, sfb = quant(to(b_bits))
             c = torch.empty((w.Ms[g], w.N), dtype=torch.float16 if nv else torch.bfloat16, device=dev)
             self.groups.append(dict(a=qa, sfa=sfa, b=qb, sfb=sfb, c=c, k=w.K))
+            if w.bf16_a:
+                self.act.append(dict(a=a16, b=qb, sfb=sfb, c=c))
         torch.cuda.synchronize()
         if nv:
             self.problems = mx.make_nv_problems(self.groups)
@@ -357,28 +365,50 @@ class NVCase:
             self.problems = mx.make_mx_problems(self.groups)
             self.call = mx.mxfp4_group_gemm
             plan = mx.mxfp4_group_gemm_plan(self.problems)
-        self.rot = 1                # ~170 MB of operands per call already exceed twice the L2
         self.launches_per_step = 1
+        if w.bf16_a:
+            self.act_problems = mx.make_nv_act_problems(self.act)
+            self.ws = torch.empty(mx.nvfp4_group_quant_gemm_workspace_bytes(self.act_problems),
+                                  dtype=torch.uint8, device=dev)
+            self.launches_per_step = 2       # grouped quantization + grouped GEMM
+        self.rot = 1                # ~170 MB of operands per call already exceed twice the L2
         self.kernel_label, self.kernel_files = kernel_of(plan, "mxf4nvf4" if nv else "mxf4")
         self.rot_bytes = w.alg_bytes
 
     def step(self, i):
+        if self.w.bf16_a:
+            self.mx.nvfp4_group_quant_gemm(self.act, self.act_problems, workspace=self.ws)
+        else:
+            self.call(self.groups, self.problems)
+
+    def prepare_gemm_only(self):
+        """The grouped GEMM alone runs on the operands quantized at set-up."""
+
+    def step_gemm_only(self, i):
         self.call(self.groups, self.problems)
 
     def alg_bytes(self):
         return self.w.alg_bytes
 
+    def gemm_alg_bytes(self):
+        return self.w.gemm_alg_bytes
+
     def e2e(self, steps, torch):
-        """Host buffers: per step copy every A_g (+ scales) in, call, copy every C_g out."""
-        pins_in = [(g["a"].cpu().pin_memory(), g["sfa"].cpu().pin_memory()) for g in self.groups]
+        """Host buffers: per step copy every A_g in (packed codes + scales, or bf16
+        with w.bf16_a), call, copy every C_g out."""
+        if self.w.bf16_a:
+            ins = [[g["a"]] for g in self.act]
+        else:
+            ins = [[g["a"], g["sfa"]] for g in self.groups]
+        pins_in = [[t.cpu().pin_memory() for t in ts] for ts in ins]
         pins_out = [torch.empty_like(g["c"], device="cpu").pin_memory() for g in self.groups]
         s = torch.cuda.current_stream()
 
         def one():
-            for (pa, ps), g in zip(pins_in, self.groups):
-                g["a"].copy_(pa, non_blocking=True)
-                g["sfa"].copy_(ps, non_blocking=True)
-            self.call(self.groups, self.problems)
+            for ps, ts in zip(pins_in, ins):
+                for p_, t in zip(ps, ts):
+                    t.copy_(p_, non_blocking=True)
+            self.step(0)
             for po, g in zip(pins_out, self.groups):
                 po.copy_(g["c"], non_blocking=True)
 
@@ -391,7 +421,7 @@ class NVCase:
             one()
         e1.record(s)
         torch.cuda.synchronize()
-        h2d = sum(pa.numel() + ps.numel() for pa, ps in pins_in)
+        h2d = sum(p_.numel() * p_.element_size() for ps in pins_in for p_ in ps)
         d2h = sum(po.numel() * 2 for po in pins_out)
         return e0.elapsed_time(e1) * 1000.0 / steps, h2d, d2h
 
@@ -480,7 +510,7 @@ def run_ours(args, name, rank, world, local_rank):
                 "frac": round(ach / fp4_peak, 4),
                 "peak_source": f"{peak_src} bf16 sustained x {FP4_OVER_BF16:g} (nominal FP4:BF16)"}
     else:
-        nbytes = case.gemm_alg_bytes() if name == "medium" else case.alg_bytes()
+        nbytes = case.gemm_alg_bytes() if case.launches_per_step > 1 else case.alg_bytes()
         ach = nbytes / (per_kernel_us * 1e-6) / 1e9
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(ach / peaks["hbm_gbs"], 4), "peak_source": f"{peak_src} hbm_gbs"}

@@ -392,6 +392,42 @@ mxfp4_status_t group_gemm_plan(const Problem *problems, int num_groups, bool nv,
     return MXFP4_OK;
 }
 
+// nvfp4_group_quant_gemm: validation of the bf16 problem list and the
+// workspace layout (per group: packed A with 16-byte rows, then its scales,
+// each at a 256-byte offset).
+struct ActWorkspace {
+    size_t aq_off[kMaxGroups], sf_off[kMaxGroups];
+    int64_t ldq[kMaxGroups];
+    size_t total;
+};
+
+mxfp4_status_t check_act_groups(const nvfp4_act_problem_t *problems, int num_groups, bool pointers,
+                                ActWorkspace *ws)
+{
+    if (!problems || num_groups < 1) return MXFP4_ERR_INVALID_ARG;
+    if (num_groups > kMaxGroups) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+    size_t off = 0;
+    for (int g = 0; g < num_groups; ++g) {
+        const nvfp4_act_problem_t &p = problems[g];
+        if (pointers && (!p.a || !p.b || !p.sfb || !p.c)) return MXFP4_ERR_INVALID_ARG;
+        if (p.m < 1 || p.n < 1 || p.k < 1 || p.m > kMaxDim || p.n > kMaxDim || p.k > kMaxDim)
+            return MXFP4_ERR_INVALID_ARG;
+        if (p.k % 16 != 0) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+        if (pointers) {
+            if (p.lda < p.k || p.ldb < p.k / 2 || p.ldc < p.n) return MXFP4_ERR_INVALID_ARG;
+            if ((p.lda * 2) % 16 != 0 || p.ldb % 16 != 0) return MXFP4_ERR_MISALIGNED;
+            if (!al16(p.a) || !al16(p.b) || !al16(p.sfb) || !al2(p.c)) return MXFP4_ERR_MISALIGNED;
+        }
+        ws->ldq[g] = (p.k / 2 + 15) / 16 * 16;
+        ws->aq_off[g] = off;
+        off += up256(static_cast<size_t>(p.m) * static_cast<size_t>(ws->ldq[g]));
+        ws->sf_off[g] = off;
+        off += up256(sf_bytes(p.m, p.k, 16));
+    }
+    ws->total = off;
+    return MXFP4_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -554,6 +590,51 @@ mxfp4_status_t nvfp4_group_gemm(const nvfp4_problem_t *problems, int num_groups,
     (void)workspace;
     (void)ws_bytes;
     return group_gemm(problems, num_groups, true, stream);
+}
+
+size_t nvfp4_group_quant_gemm_workspace_bytes(const nvfp4_act_problem_t *problems, int num_groups)
+{
+    ActWorkspace ws;
+    return check_act_groups(problems, num_groups, false, &ws) == MXFP4_OK ? ws.total : 0;
+}
+
+mxfp4_status_t nvfp4_group_quant_gemm(const nvfp4_act_problem_t *problems, int num_groups, void *workspace,
+                                      size_t ws_bytes, void *stream)
+{
+    ActWorkspace wl;
+    mxfp4_status_t st = check_act_groups(problems, num_groups, true, &wl);
+    if (st != MXFP4_OK) return st;
+    if (!workspace) return MXFP4_ERR_INVALID_ARG;
+    if (!al16(workspace)) return MXFP4_ERR_MISALIGNED;
+    if (ws_bytes < wl.total) return MXFP4_ERR_WORKSPACE_TOO_SMALL;
+    uint8_t *w = static_cast<uint8_t *>(workspace);
+    nvfp4_problem_t q[kMaxGroups];
+    QuantGroupHost qg[kMaxGroups];
+    for (int g = 0; g < num_groups; ++g) {
+        const nvfp4_act_problem_t &p = problems[g];
+        q[g].m = p.m;
+        q[g].n = p.n;
+        q[g].k = p.k;
+        q[g].a = w + wl.aq_off[g];
+        q[g].sfa = w + wl.sf_off[g];
+        q[g].b = p.b;
+        q[g].sfb = p.sfb;
+        q[g].c = p.c;
+        q[g].lda = wl.ldq[g];
+        q[g].ldb = p.ldb;
+        q[g].ldc = p.ldc;
+        qg[g] = QuantGroupHost{p.a, p.m, p.k, p.lda, w + wl.aq_off[g], wl.ldq[g], w + wl.sf_off[g]};
+    }
+    // the GEMM half's own checks, so that nothing is enqueued on a bad list
+    int64_t tiles = 0, pair_tile_count = 0;
+    st = check_groups(q, num_groups, 16, true, &tiles, &pair_tile_count);
+    if (st != MXFP4_OK) return st;
+    int sms = 0;
+    st = current_device(&sms);
+    if (st != MXFP4_OK) return st;
+    st = cuda_status(launch_quant_nv_grouped(qg, num_groups, sms, static_cast<cudaStream_t>(stream)));
+    if (st != MXFP4_OK) return st;
+    return group_gemm(q, num_groups, true, stream);
 }
 
 mxfp4_status_t mxfp4_group_gemm(const mxfp4_problem_t *problems, int num_groups, void *stream)

@@ -237,9 +237,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                         for (int h = 0; h < 2; ++h) {
                             const uint32_t pr = umax16x2(max_abs_pair8(v[x][2 * h]), max_abs_pair8(v[x][2 * h + 1]));
                             const uint32_t amax = max(pr & 0xFFFFu, pr >> 16);
-                            const uint32_t sbyte = e4m3_rn_sat(__fdiv_rn(__uint_as_float(amax << 16), 6.0f));
-                            const float sv = e4m3_value(sbyte);
-                            const uint32_t lo = nv_codes8(v[x][2 * h], sv), hi = nv_codes8(v[x][2 * h + 1], sv);
+                            const uint32_t sbyte = nv_scale_byte(amax);
+                            const float rs = nv_recip(sbyte);
+                            const uint32_t lo = nv_codes8(v[x][2 * h], rs), hi = nv_codes8(v[x][2 * h + 1], rs);
                             if (h == 0) {
                                 codes.x = lo;
                                 codes.y = hi;

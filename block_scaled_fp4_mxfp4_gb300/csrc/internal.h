@@ -15,6 +15,17 @@ cudaError_t launch_quant_mx(const void *A, int64_t M, int64_t K, int64_t lda, vo
                             int64_t ldq, void *sf, int num_sms, cudaStream_t stream);
 cudaError_t launch_quant_nv(const void *A, int64_t M, int64_t K, int64_t lda, void *Aq,
                             int64_t ldq, void *sf, int num_sms, cudaStream_t stream);
+// One matrix of a grouped NVFP4 quantization (bf16 A [M, K] -> packed codes
+// [M, K/2] with row stride ldq bytes + blocked E4M3 scales).
+struct QuantGroupHost {
+    const void *A;
+    int64_t M, K, lda;
+    void *Aq;
+    int64_t ldq;
+    void *sf;
+};
+// All `count` (1..kMaxGroups) matrices in one launch.
+cudaError_t launch_quant_nv_grouped(const QuantGroupHost *groups, int count, int num_sms, cudaStream_t stream);
 
 // ----------------------------------------------------------------- gemm.cu
 // One GEMM problem as the tile scheduler sees it.

@@ -63,20 +63,52 @@ __device__ __forceinline__ uint32_t mx_codes8(const uint4 &v, uint32_t sbyte)
     return out;
 }
 
-// Codes of 8 bf16 values divided by the decoded E4M3 scale s (fp32 division,
-// round-to-nearest-even); s == 0 leaves signed zeros.
-__device__ __forceinline__ uint32_t nv_codes8(const uint4 &v, float s)
+// NVFP4 scale byte of a 16-element group whose largest magnitude has bf16 bits
+// amax_bits: E4M3_RNE_satfinite(fp32(amax) / 6). The product amax * fp32(1/6)
+// (0x3E2AAAAB) converts to the same byte as the correctly rounded quotient for
+// every finite bf16 amax and for infinity, so no division is taken.
+__device__ __forceinline__ uint32_t nv_scale_byte(uint32_t amax_bits)
+{
+    return e4m3_rn_sat(__uint_as_float(amax_bits << 16) * __uint_as_float(0x3E2AAAABu));
+}
+
+// Reciprocal of the decoded E4M3 scale byte for nv_codes8: 1/s rounded to
+// fp32, or 0 for s == 0 (whose codes are signed zeros).
+__device__ __forceinline__ float nv_recip(uint32_t sbyte)
+{
+    const float s = e4m3_value(sbyte);
+    return s > 0.0f ? __frcp_rn(s) : 0.0f;
+}
+
+// x * (1/s) rounded onto the grid of multiples of 2^-12 by adding and
+// subtracting 3072 (= 1.5 * 2^11, whose fp32 spacing is 2^-12; the product is
+// below 1024 in magnitude wherever the code is not saturated), with x's sign
+// put back so that a negative value that rounds to zero stays -0. For a bf16 x
+// and an E4M3 s, the exact quotient x / s is either one of E2M1's rounding
+// midpoints (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5) or at least 2^-8 (relative)
+// away from every one, while x * (1/s) is within 2^-23 of it: the grid puts a
+// midpoint back exactly on itself and moves no other value across one, so the
+// E2M1 conversion of the result takes the same decision as the conversion of
+// the correctly rounded fp32 quotient. The _rn intrinsics keep the compiler
+// from fusing the multiply and the add.
+__device__ __forceinline__ float nv_snap_scaled(float x, float r)
+{
+    const float q = __fsub_rn(__fadd_rn(__fmul_rn(x, r), 3072.0f), 3072.0f);
+    return __uint_as_float(__float_as_uint(q) | (__float_as_uint(x) & 0x80000000u));
+}
+
+// Codes of 8 bf16 values divided by the decoded E4M3 scale s, given
+// r = nv_recip(scale byte): the codes of the fp32 quotients x / s rounded to
+// nearest even (see nv_snap_scaled), without a division; r == 0 (s == 0)
+// leaves signed zeros.
+__device__ __forceinline__ uint32_t nv_codes8(const uint4 &v, float r)
 {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t out = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        float flo = __uint_as_float((w[i] << 16) & 0x80000000u);
-        float fhi = __uint_as_float(w[i] & 0x80000000u);
-        if (s > 0.0f) {
-            flo = __fdiv_rn(__uint_as_float(w[i] << 16), s);
-            fhi = __fdiv_rn(__uint_as_float(w[i] & 0xFFFF0000u), s);
-        }
+        const float flo = nv_snap_scaled(__uint_as_float(w[i] << 16), r);
+        const float fhi = nv_snap_scaled(__uint_as_float(w[i] & 0xFFFF0000u), r);
         out |= e2m1x2_rn_sat(flo, fhi) << (8 * i);
     }
     return out;

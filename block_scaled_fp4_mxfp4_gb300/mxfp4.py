@@ -47,6 +47,13 @@ class MxProblem(ctypes.Structure):
     _fields_ = NvProblem._fields_
 
 
+class NvActProblem(ctypes.Structure):
+    """nvfp4_act_problem_t: a grouped NVFP4 problem with bf16 A."""
+    _fields_ = [("m", _i64), ("n", _i64), ("k", _i64),
+                ("a", _p), ("b", _p), ("sfb", _p), ("c", _p),
+                ("lda", _i64), ("ldb", _i64), ("ldc", _i64)]
+
+
 class Plan(ctypes.Structure):
     """mxfp4_plan_t: the kernel and tiling a call launches."""
     _fields_ = [("kernel", ctypes.c_int), ("tile_m", ctypes.c_int), ("tile_n", ctypes.c_int),
@@ -97,6 +104,10 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.mxfp4_gemm_plan.argtypes = [_i64, _i64, _i64, ctypes.c_int, ctypes.POINTER(Plan)]
     L.nvfp4_group_gemm_plan.restype = _st
     L.nvfp4_group_gemm_plan.argtypes = [ctypes.POINTER(NvProblem), ctypes.c_int, ctypes.POINTER(Plan)]
+    L.nvfp4_group_quant_gemm_workspace_bytes.restype = _sz
+    L.nvfp4_group_quant_gemm_workspace_bytes.argtypes = [ctypes.POINTER(NvActProblem), ctypes.c_int]
+    L.nvfp4_group_quant_gemm.restype = _st
+    L.nvfp4_group_quant_gemm.argtypes = [ctypes.POINTER(NvActProblem), ctypes.c_int, _p, _sz, _p]
     L.mxfp4_group_gemm.restype = _st
     L.mxfp4_group_gemm.argtypes = [ctypes.POINTER(MxProblem), ctypes.c_int, _p]
     L.mxfp4_group_gemm_plan.restype = _st
@@ -316,6 +327,37 @@ def nvfp4_group_gemm(groups, problems=None, stream=None):
         problems = make_nv_problems(groups)
     _check(_lib.nvfp4_group_gemm(problems, len(problems), None, 0, _stream_ptr(stream)),
            "nvfp4_group_gemm")
+    return [g["c"] for g in groups]
+
+
+def make_nv_act_problems(groups):
+    """ctypes array of nvfp4_act_problem_t from dicts with keys a (bf16 [m, k]),
+    b, sfb, c."""
+    arr = (NvActProblem * len(groups))()
+    for i, g in enumerate(groups):
+        a, b, c = g["a"], g["b"], g["c"]
+        _dev(a, "a", torch.bfloat16, 2)
+        for name, t in (("b", b), ("c", c), ("sfb", g["sfb"])):
+            _dev(t, name)
+        arr[i] = NvActProblem(a.shape[0], b.shape[0], a.shape[1], a.data_ptr(), b.data_ptr(),
+                              g["sfb"].data_ptr(), c.data_ptr(), a.stride(0), b.stride(0), c.stride(0))
+    return arr
+
+
+def nvfp4_group_quant_gemm_workspace_bytes(problems) -> int:
+    return int(_lib.nvfp4_group_quant_gemm_workspace_bytes(problems, len(problems)))
+
+
+def nvfp4_group_quant_gemm(groups, problems=None, workspace=None, stream=None):
+    """Grouped NVFP4 GEMM from bf16 activations (quantized in the call) over
+    `groups` (see make_nv_act_problems); returns the C list."""
+    if problems is None:
+        problems = make_nv_act_problems(groups)
+    if workspace is None:
+        n = nvfp4_group_quant_gemm_workspace_bytes(problems)
+        workspace = torch.empty(max(1, n), dtype=torch.uint8, device=groups[0]["a"].device)
+    _check(_lib.nvfp4_group_quant_gemm(problems, len(problems), workspace.data_ptr(), workspace.numel(),
+                                       _stream_ptr(stream)), "nvfp4_group_quant_gemm")
     return [g["c"] for g in groups]
 
 

@@ -112,18 +112,28 @@ class NVWorkload:
     K: int = 0
     seed: int = 0
     vec: int = 16
+    bf16_a: bool = False    # A_g arrives as bf16 and is quantized inside the call
 
     @property
     def flops(self) -> int:
         return sum(2 * m * self.N * self.K for m in self.Ms)
 
     @property
-    def alg_bytes(self) -> int:
+    def gemm_alg_bytes(self) -> int:
         """Packed A and B + their scales + 16-bit C, summed over groups."""
         t = 0
         for m in self.Ms:
             t += (m + self.N) * self.K // 2 + (m + self.N) * self.K // self.vec + 2 * m * self.N
         return t
+
+    @property
+    def alg_bytes(self) -> int:
+        """What one call must move: gemm_alg_bytes, or with bf16 A, the bf16 A_g in
+        place of their packed codes and scales (the quantized A_g are not counted)."""
+        if not self.bf16_a:
+            return self.gemm_alg_bytes
+        return sum(2 * m * self.K + self.N * self.K // 2 + self.N * self.K // self.vec + 2 * m * self.N
+                   for m in self.Ms)
 
 
 TINY = MXWorkload("mxfp4_tiny_M8_N512_K1024", 8, 512, 1024, "normal", 1.0, 1.0)
@@ -136,6 +146,11 @@ NVFP4_GROUPED = NVWorkload("nvfp4_grouped_8x_N4096_K7168",
 # MXFP4 (mixture-of-experts) GEMM beyond the pages' single-problem MXFP4 call.
 MXFP4_GROUPED = NVWorkload("mxfp4_grouped_8x_N4096_K7168",
                            [64, 128, 256, 384, 512, 640, 768, 1024], 4096, 7168, vec=32)
+
+# The grouped NVFP4 shapes with bf16 activations, quantized inside the call
+# (nvfp4_group_quant_gemm): dynamic NVFP4 quantization fused with the grouped GEMM.
+NVFP4_GROUPED_BF16 = NVWorkload("nvfp4_grouped_bf16a_8x_N4096_K7168",
+                                [64, 128, 256, 384, 512, 640, 768, 1024], 4096, 7168, bf16_a=True)
 
 # The decode shape with NVFP4 operands: the fused NVFP4 quant + GEMM (the NVFP4
 # twin of the fused MXFP4 path).

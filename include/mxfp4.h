@@ -214,6 +214,36 @@ MXFP4_API size_t nvfp4_group_workspace_bytes(int num_groups);
 MXFP4_API mxfp4_status_t nvfp4_group_gemm(const nvfp4_problem_t *problems, int num_groups, void *workspace,
                                 size_t ws_bytes, void *stream);
 
+/* One problem of a grouped NVFP4 GEMM whose activation is still bf16: the
+ * [NV-496271] problem list (custom_kernel) with A given unquantized, as a
+ * mixture-of-experts layer receives it. */
+typedef struct {
+    int64_t m, n, k;   /* C is [m, n]; k is the reduction length (multiple of 16) */
+    const void *a;     /* bf16 [m, k], row stride lda elements (lda * 2 a multiple of 16) */
+    const void *b;     /* uint8 [n, k/2] packed E2M1, row stride ldb bytes */
+    const void *sfb;   /* blocked E4M3 scales, mxfp4_sf_bytes(n, k, 16) bytes */
+    void *c;           /* out: fp16 [m, n], row stride ldc elements */
+    int64_t lda, ldb, ldc;
+} nvfp4_act_problem_t;
+
+/* Workspace bytes nvfp4_group_quant_gemm needs for these problems (every
+ * group's quantized A and its scales), or 0 if the list is invalid. Pointers
+ * are not read. */
+MXFP4_API size_t nvfp4_group_quant_gemm_workspace_bytes(const nvfp4_act_problem_t *problems, int num_groups);
+
+/* Dynamic NVFP4 quantization of every group's bf16 A followed by the grouped
+ * NVFP4 GEMM: one launch quantizes all A_g with nvfp4_quantize's rule and
+ * layout into the workspace, a second (in stream order) computes every C_g as
+ * nvfp4_group_gemm does from those operands. `problems` is a host array of
+ * num_groups entries (1 <= num_groups <= NVFP4_MAX_GROUPS), read during the
+ * call only. `workspace`: caller-owned device memory of at least
+ * nvfp4_group_quant_gemm_workspace_bytes bytes, 16-byte aligned; it needs no
+ * initialisation and afterwards holds the quantized A_g (layout not part of
+ * the ABI). Every argument is validated before anything is enqueued; a too
+ * small workspace gives MXFP4_ERR_WORKSPACE_TOO_SMALL. */
+MXFP4_API mxfp4_status_t nvfp4_group_quant_gemm(const nvfp4_act_problem_t *problems, int num_groups,
+                                                void *workspace, size_t ws_bytes, void *stream);
+
 /* One problem of a grouped MXFP4 GEMM: the problem list of [NV-496271]
  * custom_kernel (a, b, c, their scales, (m, n, k)) with MXFP4 operands
  * ([MM-517169]: E2M1 codes, E8M0 scale per 32 along K) and bf16 C, the layout

@@ -14,7 +14,7 @@ L = mxfp4.lib()
 
 def test_every_declared_symbol_is_exported():
     names = mxfp4.declared_symbols()
-    assert len(names) == 19
+    assert len(names) == 21
     for n in names:
         assert hasattr(L, n), n  # ctypes resolves the exported symbol
 
@@ -162,3 +162,33 @@ def test_nvfp4_fused_argument_validation_needs_no_gpu():
     assert f(16, 1024, 16, 512, 16, 16, 64, 8, 64, 1000, None) == 2      # K % 16
     assert f(None, 1024, 16, 512, 16, 16, 64, 8, 64, 1024, None) == 1
     assert f(16, 1028, 16, 512, 16, 16, 64, 8, 64, 1024, None) == 3      # lda * 2 % 16
+
+
+def test_group_quant_gemm_validation_needs_no_gpu():
+    P = mxfp4.NvActProblem
+    def one(**kw):
+        f = dict(m=64, n=256, k=512, a=16, b=16, sfb=16, c=16, lda=512, ldb=256, ldc=256)
+        f.update(kw)
+        arr = (P * 1)()
+        arr[0] = P(f["m"], f["n"], f["k"], f["a"], f["b"], f["sfb"], f["c"], f["lda"], f["ldb"], f["ldc"])
+        return arr
+    ws_fn = L.nvfp4_group_quant_gemm_workspace_bytes
+    # per group: packed A (64 rows x 256 B) then its blocked E4M3 scales (128 x 32 B), each 256-aligned
+    assert ws_fn(one(), 1) == 64 * 256 + 128 * 32
+    assert ws_fn(one(m=64, k=7168, lda=7168), 1) == 64 * 3584 + 128 * 448
+    two = (P * 2)()
+    two[0], two[1] = one()[0], one(m=3, k=48, lda=48)[0]   # 3 x 24 B rows -> 16-byte rows of 32 B
+    assert ws_fn(two, 2) == (64 * 256 + 128 * 32) + (256 + 512)
+    assert ws_fn(one(k=40, lda=40), 1) == 0                # K % 16
+    f = L.nvfp4_group_quant_gemm
+    big = 1 << 30
+    assert f(one(k=40, lda=40), 1, 16, big, None) == 2
+    assert f(one(a=0), 1, 16, big, None) == 1
+    assert f(one(lda=500), 1, 16, big, None) == 1          # lda < k
+    assert f(one(lda=516), 1, 16, big, None) == 3          # lda * 2 % 16
+    assert f(one(a=24), 1, 16, big, None) == 3             # A not 16-byte aligned
+    assert f(one(), 1, None, big, None) == 1               # no workspace
+    assert f(one(), 1, 24, big, None) == 3                 # workspace alignment
+    assert f(one(), 1, 16, 64 * 256, None) == 4            # workspace too small
+    assert f(one(), 17, 16, big, None) == 2                # too many groups
+    assert f(None, 1, 16, big, None) == 1

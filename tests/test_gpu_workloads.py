@@ -132,3 +132,28 @@ def test_mxfp4_grouped_sampled():
         got = gd["c"][torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].float().cpu().numpy()
         assert_within_tolerance(got.astype(np.float64), c_ref, s, f"mxfp4 group {g} (sampled)")
     assert mx.get_device_error() == 0
+
+
+def test_nvfp4_grouped_bf16_sampled():
+    """The bf16-activation grouped call bench.py times: C_g sampled against the
+    oracle, which quantizes the same bf16 A_g itself."""
+    w = wl.NVFP4_GROUPED_BF16
+    groups, refs = [], []
+    for g in range(len(w.Ms)):
+        a_bits, b_bits = wl.gen_nv_group(w, g)
+        qb, sfb = mx.nvfp4_quantize(dev_bf16(b_bits))
+        c = torch.full((w.Ms[g], w.N), float("nan"), dtype=torch.float16, device="cuda")
+        groups.append(dict(a=dev_bf16(a_bits), b=qb, sfb=sfb, c=c))
+        refs.append((a_bits, b_bits))
+    problems = mx.make_nv_act_problems(groups)
+    mx.nvfp4_group_quant_gemm(groups, problems)
+    torch.cuda.synchronize()
+    for g, (gd, (a_bits, b_bits)) in enumerate(zip(groups, refs)):
+        qa_r, sfa_r = oracle.nv_quantize(a_bits)
+        qb_r, sfb_r = oracle.nv_quantize(b_bits)
+        assert_bytes_equal(host(gd["b"]), qb_r, f"group {g} B codes")
+        rows, cols = sample_pairs(w.Ms[g], w.N, 2048, 1, 1, seed=80 + g)
+        c_ref, s = oracle.gemm_sampled(qa_r, sfa_r, qb_r, sfb_r, w.K, 16, rows, cols)
+        got = gd["c"][torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].float().cpu().numpy()
+        assert_within_tolerance(got.astype(np.float64), c_ref, s, f"nvfp4 bf16-A group {g} (sampled)")
+    assert mx.get_device_error() == 0
