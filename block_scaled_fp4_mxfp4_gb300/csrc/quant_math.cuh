@@ -15,6 +15,24 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void *p)
     return v;
 }
 
+// E2M1 codes of 8 values packed into 32 bits, x0 in the low nibble of byte 0
+// and x7 in the high nibble of byte 3 (round to nearest even, saturating, sign
+// kept); the four converted bytes are packed by one vector move.
+__device__ __forceinline__ uint32_t e2m1x8_rn_sat(float x0, float x1, float x2, float x3, float x4, float x5,
+                                                  float x6, float x7)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b8 c0, c1, c2, c3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 c0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 c1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 c2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 c3, %8, %7;\n\t"
+        "mov.b32 %0, {c0, c1, c2, c3};\n\t}"
+        : "=r"(r)
+        : "f"(x0), "f"(x1), "f"(x2), "f"(x3), "f"(x4), "f"(x5), "f"(x6), "f"(x7));
+    return r;
+}
+
 // Lane-wise unsigned 16-bit max of two packed pairs.
 __device__ __forceinline__ uint32_t umax16x2(uint32_t a, uint32_t b)
 {
@@ -53,14 +71,13 @@ __device__ __forceinline__ uint32_t mx_codes8(const uint4 &v, uint32_t sbyte)
 {
     const float mult = __uint_as_float((254u - sbyte) << 23);  // 2^-e, e = sbyte - 127
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t out = 0;
+    float f[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const float flo = __uint_as_float(w[i] << 16) * mult;
-        const float fhi = __uint_as_float(w[i] & 0xFFFF0000u) * mult;
-        out |= e2m1x2_rn_sat(flo, fhi) << (8 * i);
+        f[2 * i] = __uint_as_float(w[i] << 16) * mult;
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u) * mult;
     }
-    return out;
+    return e2m1x8_rn_sat(f[0], f[1], f[2], f[3], f[4], f[5], f[6], f[7]);
 }
 
 // NVFP4 scale byte of a 16-element group whose largest magnitude has bf16 bits
@@ -104,14 +121,13 @@ __device__ __forceinline__ float nv_snap_scaled(float x, float r)
 __device__ __forceinline__ uint32_t nv_codes8(const uint4 &v, float r)
 {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t out = 0;
+    float f[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const float flo = nv_snap_scaled(__uint_as_float(w[i] << 16), r);
-        const float fhi = nv_snap_scaled(__uint_as_float(w[i] & 0xFFFF0000u), r);
-        out |= e2m1x2_rn_sat(flo, fhi) << (8 * i);
+        f[2 * i] = nv_snap_scaled(__uint_as_float(w[i] << 16), r);
+        f[2 * i + 1] = nv_snap_scaled(__uint_as_float(w[i] & 0xFFFF0000u), r);
     }
-    return out;
+    return e2m1x8_rn_sat(f[0], f[1], f[2], f[3], f[4], f[5], f[6], f[7]);
 }
 
 }  // namespace mxfp4
