@@ -18,7 +18,13 @@ it restates. Parity pins:
 * The NVFP4 *quantization* rule (E4M3 scale = RNE(amax/6)) is a reading: the
   pages consume NVFP4 operands but do not print the producer's rule. Its
   codecs are pinned; the rule as a whole is "parity unpinned" beyond them.
+* The fused RMSNorm + MXFP4 quantization (``rmsnorm_y``,
+  ``rmsnorm_mx_quantize``) is a reading too (the pages name the fused
+  operation, not its arithmetic); it is pinned by its reduction to the plain
+  MXFP4 quantizer on rows whose norm is a power of two, by scale invariance,
+  by closed forms and by a high-precision evaluation of y.
 """
+import math
 import ctypes
 import os
 
@@ -257,3 +263,56 @@ def check_tolerance(c_gpu, c_ref, s_abs):
     worst = np.zeros(1, dtype=np.float64)
     bad = lib().orc_check_tolerance(_ptr(cg), _ptr(cr), _ptr(sa), cg.size, _ptr(worst))
     return int(bad), float(worst[0])
+
+
+# ------------------------------------------------ RMSNorm + MXFP4 quantize --
+
+def _bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    return (np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def rmsnorm_y(X_bits: np.ndarray, w_bits: np.ndarray, eps: float) -> np.ndarray:
+    """Normalized rows y [M, K] (float32) of the fused RMSNorm + MXFP4
+    quantization. The source pages (kernelbot-amd-mxfp4-mm-683203, the fused
+    RMSNorm + MXFP4 quantization kernel its activation path cites) name the
+    operation without its arithmetic; the reading taken, for bf16 x [K] and a
+    bf16 weight w [K]:
+      ss  = sum_k x_k^2, the exact sum (each square is exact in fp64; math.fsum
+            rounds the exact total once)
+      r64 = 1 / sqrt(ss / K + eps) in fp64, or 0 when ss / K + eps == 0
+      r   = fp32(r64)
+      y_k = fp32(fp32(x_k * r) * w_k)
+    with eps the caller's fp32 value."""
+    X = _bf16_bits_to_f64(X_bits)
+    w32 = _bf16_bits_to_f64(w_bits).astype(np.float32)
+    M, K = X.shape
+    assert w32.shape == (K,)
+    e = float(np.float32(eps))
+    y = np.empty((M, K), dtype=np.float32)
+    for m in range(M):
+        row = X[m]
+        ss = math.fsum((row * row).tolist())
+        d = ss / K + e
+        r = np.float32(0.0 if d == 0.0 else 1.0 / math.sqrt(d))
+        y[m] = (row.astype(np.float32) * r).astype(np.float32) * w32
+    return y
+
+
+def rmsnorm_mx_quantize(X_bits: np.ndarray, w_bits: np.ndarray, eps: float):
+    """bf16 X [M, K], bf16 w [K] -> (packed E2M1 codes [M, K/2], blocked E8M0
+    scales) of y = rmsnorm_y(X, w, eps), each 32-value block of y quantized by
+    the OCP MX rule exactly as mx_quantize_block does (scale pad 0x7F)."""
+    y = rmsnorm_y(X_bits, w_bits, eps)
+    M, K = y.shape
+    if K % 32:
+        raise ValueError(f"K={K} is not a multiple of 32")
+    C = K // 32
+    q = np.zeros((M, K // 2), dtype=np.uint8)
+    lin = np.zeros((M, C), dtype=np.uint8)
+    for m in range(M):
+        for b in range(C):
+            sb, codes = mx_quantize_block(y[m, 32 * b:32 * b + 32].astype(np.float64))
+            lin[m, b] = sb
+            c = np.asarray(codes, dtype=np.uint8) & 15
+            q[m, 16 * b:16 * b + 16] = c[0::2] | (c[1::2] << 4)
+    return q, sf_pack(lin, 127)

@@ -447,3 +447,84 @@ def test_epilogue_is_linear_in_alpha_and_beta():
     assert np.array_equal(two, 2.0 * one)
     with_c, _ = oracle.gemm_epilogue(c, s, 1.0, 0.25, c_in)
     assert np.allclose(with_c - one, 0.25 * c_in, rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------- RMSNorm + MXFP4 (reading) --
+
+def _bits(x):
+    return wl.to_bf16_bits(np.asarray(x, dtype=np.float64))
+
+
+def test_rmsnorm_on_power_of_two_rows_is_the_plain_quantizer_of_w():
+    # rows of +-2^j: sum x^2 / K = 4^j exactly, r = 2^-j, y = sign(x) * w exactly,
+    # so the fused output must equal the plain MXFP4 quantizer applied to sign(x) * w
+    K = 96
+    w = wl.gen_bf16(7, 1, 1, K)[0]
+    wv = oracle._bf16_bits_to_f64(w)
+    rng = np.random.default_rng(3)
+    rows, want_rows = [], []
+    for j in (-20, -3, 0, 1, 9, 60):
+        sign = np.where(rng.random(K) < 0.5, -1.0, 1.0)
+        rows.append(sign * 2.0 ** j)
+        want_rows.append(sign * wv)
+    q, sf = oracle.rmsnorm_mx_quantize(_bits(rows), w, 0.0)
+    q_ref, sf_ref = oracle.mx_quantize(_bits(want_rows))
+    assert np.array_equal(q, q_ref) and np.array_equal(sf, sf_ref)
+
+
+def test_rmsnorm_is_scale_invariant_without_eps():
+    X = wl.gen_bf16(8, 2, 5, 128)
+    w = wl.gen_bf16(8, 3, 1, 128)[0]
+    q1, s1 = oracle.rmsnorm_mx_quantize(X, w, 0.0)
+    X4 = _bits(oracle._bf16_bits_to_f64(X) * 4.0)      # exact in bf16
+    q2, s2 = oracle.rmsnorm_mx_quantize(X4, w, 0.0)
+    assert np.array_equal(q1, q2) and np.array_equal(s1, s2)
+    # a bias in the mean (dividing by K - 1, say) or a dropped square root breaks this pin
+    y = oracle.rmsnorm_y(X, w, 0.0)
+    assert not np.array_equal(y, oracle.rmsnorm_y(X4, w, 0.0) * 0.5)
+
+
+def test_rmsnorm_constant_rows_closed_form():
+    # x = c = 2^j everywhere, w = 1, eps tiny: r = 2^-j, y = 1, amax 1 -> scale
+    # 2^-2 (byte 125), every code 4.0 (index 6); -c gives 0xE
+    K = 64
+    w = _bits(np.ones(K))
+    X = _bits([np.full(K, 2.0 ** 5), np.full(K, -(2.0 ** -7))])
+    q, sf = oracle.rmsnorm_mx_quantize(X, w, 1e-30)
+    assert np.all(q[0] == 0x66) and np.all(q[1] == 0xEE)
+    lin = oracle.sf_unpack(sf, 2, K // 32)
+    assert np.all(lin == 125)
+
+
+def test_rmsnorm_zero_row_without_eps_gives_signed_zeros():
+    K = 32
+    X = np.zeros((1, K), dtype=np.uint16)
+    X[0, 3] = 0x8000                                     # -0
+    w = _bits(np.where(np.arange(K) % 2 == 0, 1.0, -1.0))
+    q, sf = oracle.rmsnorm_mx_quantize(X, w, 0.0)
+    codes = np.stack([q[0] & 15, q[0] >> 4], axis=1).ravel()
+    # y = (x * 0) * w: +0 * w has w's sign, -0 * w the opposite
+    want = np.where(np.arange(K) % 2 == 0, 0, 8)
+    want[3] ^= 8
+    assert np.array_equal(codes, want)
+    assert oracle.sf_unpack(sf, 1, 1)[0, 0] == 0
+
+
+def test_rmsnorm_y_matches_a_high_precision_evaluation():
+    # three fp32 roundings (r, x*r, *w) bound the error of y by ~3 ulp
+    from decimal import Decimal, getcontext
+    getcontext().prec = 60
+    X = wl.gen_bf16(9, 4, 4, 160)
+    w = wl.gen_bf16(9, 5, 1, 160)[0]
+    for eps in (0.0, 1e-6, 0.75):
+        y = oracle.rmsnorm_y(X, w, eps)
+        Xd = oracle._bf16_bits_to_f64(X)
+        wd = oracle._bf16_bits_to_f64(w)
+        e = Decimal(float(np.float32(eps)))
+        for m in range(X.shape[0]):
+            ms = sum(Decimal(float(v)) ** 2 for v in Xd[m]) / Decimal(X.shape[1]) + e
+            r = 1 / ms.sqrt()
+            for k in range(X.shape[1]):
+                exact = Decimal(float(Xd[m, k])) * r * Decimal(float(wd[k]))
+                err = abs(Decimal(float(y[m, k])) - exact)
+                assert err <= Decimal(3.01) * Decimal(2) ** -24 * abs(exact), (eps, m, k)
