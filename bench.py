@@ -9,6 +9,7 @@ A step is one call of the hot path on one batch of synthetic input:
   nvfp4_decode      nvfp4_quant_gemm_fused on the decode shape (NVFP4 operands, fp16 C)
   nvfp4_grouped_bf16  nvfp4_group_quant_gemm: the nvfp4_grouped shapes with bf16 A_g,
                     quantized inside every call (grouped quantization + grouped GEMM)
+  rmsnorm_decode / rmsnorm_prefill  mxfp4_rmsnorm_quantize on bf16 X [16 | 4096, 7168]
 Weights are pre-quantized once, untimed, by the library's own quantizer.
 
 Prints one JSON line (rank 0). `value` is microseconds per call over the whole
@@ -52,14 +53,22 @@ WORKLOADS = {
     "mxfp4_grouped": wl.MXFP4_GROUPED,
     "nvfp4_decode": wl.NVFP4_DECODE,
     "nvfp4_grouped_bf16": wl.NVFP4_GROUPED_BF16,
+    "rmsnorm_decode": wl.RMSNORM_DECODE,
+    "rmsnorm_prefill": wl.RMSNORM_PREFILL,
 }
 DEFAULT_STEPS = {"decode": 20000, "tiny": 20000, "medium": 10000, "compute": 50, "nvfp4_grouped": 500,
-                 "mxfp4_grouped": 500, "nvfp4_decode": 20000, "nvfp4_grouped_bf16": 500}
+                 "mxfp4_grouped": 500, "nvfp4_decode": 20000, "nvfp4_grouped_bf16": 500,
+                 "rmsnorm_decode": 20000, "rmsnorm_prefill": 1000}
 
 
 def grouped(name):
     """Whether a workload is a grouped GEMM (NVFP4 or MXFP4)."""
     return isinstance(WORKLOADS[name], wl.NVWorkload)
+
+
+def rmsnorm(name):
+    """Whether a workload is the fused RMSNorm + MXFP4 quantization."""
+    return isinstance(WORKLOADS[name], wl.RMSWorkload)
 
 
 def max_over_ranks(value, world, device):
@@ -113,6 +122,7 @@ KERNEL_SOURCES = {
     "fused_quant_gemm_kernel": ["fused.cu", "ptx.cuh", "quant_math.cuh"],
     "bs_gemm_kernel": ["gemm.cu", "gemm_common.cuh", "ptx.cuh"],
     "bs_gemm_pair_kernel": ["gemm_pair.cu", "gemm_common.cuh", "ptx.cuh"],
+    "rmsnorm_mx_quant_kernel": ["rmsnorm_quant.cu", "quant_math.cuh", "ptx.cuh"],
 }
 
 
@@ -426,6 +436,60 @@ class NVCase:
         return e0.elapsed_time(e1) * 1000.0 / steps, h2d, d2h
 
 
+class RMSCase:
+    """Fused RMSNorm + MXFP4 quantization of resident bf16 activations
+    (mxfp4_rmsnorm_quantize), rotating over copies of X to defeat the L2."""
+
+    def __init__(self, w, dev, mx, torch):
+        self.w, self.mx, self.torch = w, mx, torch
+        x_bits, g_bits = wl.gen_rms(w)
+        to = lambda bits: torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        X0 = to(x_bits)
+        self.weight = to(g_bits)
+        per = w.alg_bytes
+        l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20)
+        self.rot = max(1, min(64, math.ceil(2 * l2 / per)))
+        self.X = [X0] + [X0.clone() for _ in range(self.rot - 1)]
+        self.Aq, self.sf = mx.mxfp4_rmsnorm_quantize(X0, self.weight, w.eps)
+        torch.cuda.synchronize()
+        self.launches_per_step = 1
+        rows = (w.M + 127) // 128 * 128
+        self.kernel_label = f"rmsnorm_mx_quant_kernel x{rows} rows (one CTA per row)"
+        self.kernel_files = KERNEL_SOURCES["rmsnorm_mx_quant_kernel"]
+        self.rot_bytes = per * self.rot
+
+    def step(self, i):
+        self.mx.mxfp4_rmsnorm_quantize(self.X[i % self.rot], self.weight, self.w.eps, self.Aq, self.sf)
+
+    def alg_bytes(self):
+        return self.w.alg_bytes
+
+    def e2e(self, steps, torch):
+        """Host buffers: per step copy X in, call, copy the codes and scales out."""
+        pin_x = self.X[0].cpu().pin_memory()
+        pin_q = torch.empty_like(self.Aq, device="cpu").pin_memory()
+        pin_s = torch.empty_like(self.sf, device="cpu").pin_memory()
+        s = torch.cuda.current_stream()
+
+        def one():
+            self.X[0].copy_(pin_x, non_blocking=True)
+            self.step(0)
+            pin_q.copy_(self.Aq, non_blocking=True)
+            pin_s.copy_(self.sf, non_blocking=True)
+
+        for _ in range(3):
+            one()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(steps):
+            one()
+        e1.record(s)
+        torch.cuda.synchronize()
+        return (e0.elapsed_time(e1) * 1000.0 / steps, pin_x.numel() * 2,
+                pin_q.numel() + pin_s.numel())
+
+
 def run_ours(args, name, rank, world, local_rank):
     import torch
     from block_scaled_fp4_mxfp4_gb300 import mxfp4 as mx
@@ -435,7 +499,10 @@ def run_ours(args, name, rank, world, local_rank):
     w = WORKLOADS[name]
     steps = args.steps if args.steps is not None else DEFAULT_STEPS[name]
     warmup = args.warmup if args.warmup is not None else max(3, min(100, steps // 10))
-    case = NVCase(w, dev, mx, torch) if grouped(name) else MXCase(w, dev, mx, torch)
+    if rmsnorm(name):
+        case = RMSCase(w, dev, mx, torch)
+    else:
+        case = NVCase(w, dev, mx, torch) if grouped(name) else MXCase(w, dev, mx, torch)
 
     for i in range(max(warmup, case.rot)):  # warm-up (also encodes every TMA descriptor once)
         case.step(i)
@@ -560,7 +627,9 @@ def _oracle_prep(name):
     if name in _ORACLE_PREP:
         return _ORACLE_PREP[name]
     w = WORKLOADS[name]
-    if grouped(name):
+    if rmsnorm(name):
+        prep = wl.gen_rms(w)
+    elif grouped(name):
         quant = oracle.nv_quantize if w.vec == 16 else oracle.mx_quantize
         prep = []
         for g in range(len(w.Ms)):
@@ -579,6 +648,17 @@ def oracle_call_sampled(name, budget_s):
     """Time the oracle on a bounded sample of one call; return (us per full call, sample text)."""
     import oracle
     w = WORKLOADS[name]
+    if rmsnorm(name):
+        x_bits, g_bits = _oracle_prep(name)
+        t0 = time.perf_counter()
+        oracle.rmsnorm_mx_quantize(x_bits[:1], g_bits, w.eps)
+        per_row = time.perf_counter() - t0
+        r = max(1, min(w.M, int(budget_s / per_row)))
+        t0 = time.perf_counter()
+        oracle.rmsnorm_mx_quantize(x_bits[:r], g_bits, w.eps)
+        dt = time.perf_counter() - t0
+        full = "the full call" if r == w.M else f"rows 0..{r - 1} of {w.M}, scaled by rows"
+        return dt / r * w.M * 1e6, f"{full} (exact sum of squares, fp32 y, OCP MX blocks)"
     if grouped(name):
         # sample: the first r rows of every group, all N columns
         quant = oracle.nv_quantize if w.vec == 16 else oracle.mx_quantize

@@ -156,6 +156,40 @@ NVFP4_GROUPED_BF16 = NVWorkload("nvfp4_grouped_bf16a_8x_N4096_K7168",
 # twin of the fused MXFP4 path).
 NVFP4_DECODE = MXWorkload("nvfp4_decode_M16_N2112_K7168", 16, 2112, 7168, "normal", 1.0, 0.02, vec=16)
 
+
+
+@dataclass
+class RMSWorkload:
+    """Fused RMSNorm + MXFP4 quantization: bf16 X [M, K] (N(0, 1)), bf16 weight
+    [K] (1 + N(0, 0.1)), eps."""
+    name: str
+    M: int
+    K: int
+    eps: float = 1e-6
+    seed: int = 0
+
+    @property
+    def flops(self) -> int:
+        return 4 * self.M * self.K      # square, add, two products per element
+
+    @property
+    def alg_bytes(self) -> int:
+        """bf16 X + bf16 weight + packed codes + E8M0 scales."""
+        return 2 * self.M * self.K + 2 * self.K + self.M * self.K // 2 + self.M * self.K // 32
+
+
+def gen_rms(w: "RMSWorkload"):
+    """bf16 bits of (X [M, K], weight [K])."""
+    x = normal(stream_key(w.seed, 40), w.M * w.K)
+    g = 1.0 + 0.1 * normal(stream_key(w.seed, 41), w.K)
+    return to_bf16_bits(x).reshape(w.M, w.K), to_bf16_bits(g)
+
+
+# The activation rows of the decode GEMM (16 x 7168) and a prefill-sized batch,
+# normalized and quantized in one call ahead of the MXFP4 GEMM.
+RMSNORM_DECODE = RMSWorkload("mxfp4_rmsnorm_quant_M16_K7168", 16, 7168)
+RMSNORM_PREFILL = RMSWorkload("mxfp4_rmsnorm_quant_M4096_K7168", 4096, 7168)
+
 MX_WORKLOADS = {w.name: w for w in (TINY, DECODE, MEDIUM, COMPUTE)}
 
 # tensor ids inside a workload's seed

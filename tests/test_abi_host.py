@@ -14,7 +14,7 @@ L = mxfp4.lib()
 
 def test_every_declared_symbol_is_exported():
     names = mxfp4.declared_symbols()
-    assert len(names) == 21
+    assert len(names) == 22
     for n in names:
         assert hasattr(L, n), n  # ctypes resolves the exported symbol
 
@@ -192,3 +192,19 @@ def test_group_quant_gemm_validation_needs_no_gpu():
     assert f(one(), 1, 16, 64 * 256, None) == 4            # workspace too small
     assert f(one(), 17, 16, big, None) == 2                # too many groups
     assert f(None, 1, 16, big, None) == 1
+
+
+def test_rmsnorm_quantize_validation_needs_no_gpu():
+    f = L.mxfp4_rmsnorm_quantize
+    ok = dict(X=16, M=4, K=64, ldx=64, w=16, eps=1e-6, Aq=16, ldq=32, sf=16)
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["X"], a["M"], a["K"], a["ldx"], a["w"], a["eps"], a["Aq"], a["ldq"], a["sf"], None)
+    assert call(K=48, ldx=48, ldq=24) == 2      # K % 32
+    assert call(w=None) == 1
+    assert call(eps=-1.0) == 1
+    assert call(eps=float("nan")) == 1
+    assert call(eps=float("inf")) == 1
+    assert call(w=24) == 3                      # weight alignment
+    assert call(ldx=68) == 3                    # ldx * 2 % 16
+    assert call(X=None) == 1
