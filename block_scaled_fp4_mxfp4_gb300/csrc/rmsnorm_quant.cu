@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(kRmsThreads) rmsnorm_mx_quant_kernel(const uin
                                                                        float eps, uint8_t *__restrict__ Aq,
                                                                        int64_t ldq, uint8_t *__restrict__ sf)
 {
-    __shared__ int s_emax[kRmsWarps];
+    __shared__ int s_emax[kRmsWarps];       // per-warp largest magnitude (bf16 bits)
     __shared__ unsigned long long s_lo[kRmsWarps], s_hi[kRmsWarps];
     __shared__ float s_r;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -105,39 +105,42 @@ __global__ void __launch_bounds__(kRmsThreads) rmsnorm_mx_quant_kernel(const uin
         const uint16_t *xrow = X + r * ldx;
         float rs = 0.0f;
         if (row_ok) {
-            // pass 1: the largest exponent among the row's nonzero elements
-            int emax = 0;
-            for (int i = tid; i < nvec; i += kRmsThreads) {
-                const uint4 v = ld_nc_v4(xrow + i * 8);
-                const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    int e;
-                    uint32_t m;
-                    bf16_parts((wv[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu, e, m);
-                    if (m != 0 && e > emax) emax = e;
-                }
-            }
-            emax = __reduce_max_sync(0xffffffffu, static_cast<unsigned>(emax));
-            if (lane == 0) s_emax[warp] = emax;
+            // pass 1: the largest magnitude of the row (bf16 magnitudes order as integers)
+            uint32_t mm = 0;
+            for (int i = tid; i < nvec; i += kRmsThreads) mm = max(mm, max_abs_bits8(ld_nc_v4(xrow + i * 8)));
+            mm = __reduce_max_sync(0xffffffffu, mm);
+            if (lane == 0) s_emax[warp] = static_cast<int>(mm);
             __syncthreads();
-            emax = 0;
+            mm = 0;
 #pragma unroll
-            for (int i = 0; i < kRmsWarps; ++i) emax = max(emax, s_emax[i]);
-            // pass 2: exact sum of squares at the common exponent
+            for (int i = 0; i < kRmsWarps; ++i) mm = max(mm, static_cast<uint32_t>(s_emax[i]));
+            // its exponent (1 for subnormals, 0 for an all-zero row)
+            const int emax = mm ? max(static_cast<int>(mm >> 7), 1) : 0;
+            // pass 2: exact sum of squares at the common exponent. A square whose
+            // shift is at least 48 (|x| within 2^16 of the largest) goes to a
+            // 64-bit per-vector sum (< 8 * 2^48), added to the 128-bit
+            // accumulator once per vector; smaller ones take the general path.
+            const int base = kRmsHeadroom - 2 * emax;
             U128 acc{0ull, 0ull};
             for (int i = tid; i < nvec; i += kRmsThreads) {
                 const uint4 v = ld_nc_v4(xrow + i * 8);
                 const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+                unsigned long long fast = 0;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     int e;
                     uint32_t m;
                     bf16_parts((wv[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu, e, m);
-                    unsigned long long lo, hi;
-                    square_term(m, 2 * (e - emax) + kRmsHeadroom, lo, hi);
-                    add128(acc, lo, hi);
+                    const int sh = 2 * e + base;
+                    if (sh >= 48) {
+                        fast += static_cast<unsigned long long>(m * m) << (sh - 48);
+                    } else if (m != 0) {
+                        unsigned long long lo, hi;
+                        square_term(m, sh, lo, hi);
+                        add128(acc, lo, hi);
+                    }
                 }
+                add128(acc, fast << 48, fast >> 16);
             }
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) {
