@@ -1,6 +1,7 @@
 """bench.py's multi-rank bookkeeping on CPU: world_size-2 gloo ranks agree on
 the slowest rank's time and on the whole-job time per call; a non-zero rank of
 the reference arm exits without work. No GPU."""
+import json
 import os
 import subprocess
 import sys
@@ -61,3 +62,18 @@ def test_reference_arm_runs_on_rank_zero_only():
                        env=env, capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+@pytest.mark.parametrize("workload", ["tiny", "rmsnorm_decode"])
+def test_reference_arm_prints_the_contract_line(workload):
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                        workload, "--steps", "1", "--warmup", "0"],
+                       env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["steps"] == 1 and line["value"] > 0
+    assert line["higher_is_better"] is False and line["unit"] == "us/call"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "us/call", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
