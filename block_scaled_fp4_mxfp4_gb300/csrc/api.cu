@@ -15,6 +15,19 @@ using namespace mxfp4;
 
 namespace {
 
+std::atomic<uint64_t> g_wait_limit_ns{kWaitTimeoutNs};
+
+}  // namespace
+
+namespace mxfp4 {
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+void set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : kWaitTimeoutNs, std::memory_order_relaxed); }
+
+}  // namespace mxfp4
+
+namespace {
+
 // Split-K and path plans assume this many SMs so that the workspace size is a
 // function of the shape alone (GB300 has 152; fewer SMs only change occupancy).
 constexpr int kPlanSms = 152;
@@ -696,6 +709,13 @@ mxfp4_status_t mxfp4_group_gemm_plan(const mxfp4_problem_t *problems, int num_gr
     return group_gemm_plan(problems, num_groups, false, out);
 }
 
+uint64_t mxfp4_set_wait_limit_ns(uint64_t ns)
+{
+    const uint64_t old = wait_limit_ns();
+    set_wait_limit_ns(ns);
+    return old;
+}
+
 mxfp4_status_t mxfp4_get_device_error(int *code)
 {
     if (!code) return MXFP4_ERR_INVALID_ARG;
@@ -725,17 +745,24 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 std::mutex g_noalloc_mu;
 void *g_noalloc_ptr[64] = {};
 
-// Device address of the scratch array on the current device, looked up once
-// per device (host code only sees a stand-in symbol, never the address).
-mxfp4_status_t noalloc_scratch(void **out)
+// Device address of the scratch array on the current device (host code only
+// sees a stand-in symbol, never the address). Looked up again on every call
+// made outside stream capture, so that a device reset or a new primary
+// context never leaves a stale address behind; a call made while `stream` is
+// being captured uses the address of the last call on that device.
+mxfp4_status_t noalloc_scratch(cudaStream_t stream, void **out)
 {
     int d = 0;
     if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64) return MXFP4_ERR_NO_DEVICE;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return MXFP4_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_ptr[d]) {
+    if (cap == cudaStreamCaptureStatusNone) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MXFP4_ERR_CUDA;
         g_noalloc_ptr[d] = p;
+    } else if (!g_noalloc_ptr[d]) {
+        return MXFP4_ERR_CUDA;   // the first call on a device must come before any capture
     }
     *out = g_noalloc_ptr[d];
     return MXFP4_OK;
@@ -770,10 +797,10 @@ mxfp4_status_t mxfp4_gemm_a4w4_noalloc(const void *Aq, int64_t ldaq, const void 
     int sms = 0;
     st = current_device(&sms);
     if (st != MXFP4_OK) return st;
-    void *scratch = nullptr;
-    st = noalloc_scratch(&scratch);
-    if (st != MXFP4_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *scratch = nullptr;
+    st = noalloc_scratch(s, &scratch);
+    if (st != MXFP4_OK) return st;
     // the tile tickets must start at zero; the array keeps whatever the last call left
     if (cudaMemsetAsync(static_cast<uint8_t *>(scratch) + wl.ticket_off, 0, static_cast<size_t>(gp.tiles) * 4, s) !=
         cudaSuccess)

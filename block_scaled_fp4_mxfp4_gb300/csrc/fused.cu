@@ -83,7 +83,8 @@ struct FusedCfg {
     static_assert(ACT_TILE % 1024 == 0, "swizzled operand tiles need 1024-byte alignment");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(ACC_COLS + MAX_ST * SF_COLS <= 512, "TMEM budget");
-    static_assert((2 * kRing + 1) * 8 + 8 <= 256, "barrier area");
+    // full, empty per ring slot, accf; TMEM address, abort flag, every peer's abort flag
+    static_assert((2 * kRing + 1) * 8 + 8 + kMaxSplits * 4 <= 256, "barrier area");
 };
 
 struct FusedArgs {
@@ -95,6 +96,7 @@ struct FusedArgs {
     int M, N, K;
     int splits;
     int sf_cblocks;
+    uint64_t wait_ns;     // limit of the waits that guard work
 };
 
 // C element from fp32: bf16 (MXFP4) or fp16 (NVFP4), round to nearest even.
@@ -123,7 +125,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint64_t *empty = full + kRing;
     uint64_t *accf = empty + kRing;              // one arrival per stage warp
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accf + 1);
-    int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
+    volatile int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
+    volatile int *abort_in = abort_flag + 1;    // [kMaxSplits] the abort flag of each CTA of the cluster
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -188,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             // ------------------------------- weight TMA producer (stages past the ring)
             for (int i = kRing; i < nst; ++i) {
                 const int slot = i % kRing;
-                if (!mbar_wait(empty + slot, ((i / kRing) - 1) & 1, &g_fused_error, kErrWaitEmpty)) {
+                if (!mbar_wait(empty + slot, ((i / kRing) - 1) & 1, &g_fused_error, kErrWaitEmpty, p.wait_ns)) {
                     *abort_flag = 1;
                     break;
                 }
@@ -267,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             __syncwarp();
             if (lane == 0) {
                 const int slot = t % kRing;
-                if (!mbar_wait(full + slot, (t / kRing) & 1, &g_fused_error, kErrWaitFull)) {
+                if (!mbar_wait(full + slot, (t / kRing) & 1, &g_fused_error, kErrWaitFull, p.wait_ns)) {
                     *abort_flag = 1;
                 } else {
                     tc_fence_after();
@@ -316,7 +319,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int nper = (128 + S - 1) / S;           // weight rows each CTA of the cluster owns
     const int nacc = min(nst, kStageWarps);       // accumulators that hold data
     if (warp >= 2) {
-        const bool acc_ok = mbar_wait(accf, 0, &g_fused_error, kErrWaitAccum);
+        // a stage warp that gave up set the abort flag before its arrival on accf
+        const bool acc_ok = mbar_wait(accf, 0, &g_fused_error, kErrWaitAccum, p.wait_ns) && *abort_flag == 0;
         // The next grid in the stream may start once the accumulators are
         // complete. Its weight stream then overlaps this grid's reduction and
         // exit instead of competing with this grid's loads of A (measured on
@@ -362,11 +366,20 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 
     if (S > 1) {
-        // every CTA of the cluster reaches the barrier, also after an abort
+        // Every CTA tells every CTA of the cluster whether it gave up: an owner
+        // whose slice misses a partial sum leaves C unwritten (the call then
+        // reports the device error). Every CTA reaches the barrier, also after
+        // an abort.
+        __syncthreads();
+        if (threadIdx.x < S)
+            st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int *>(abort_in + split)), threadIdx.x),
+                                  static_cast<uint32_t>(*abort_flag));
         cluster_sync();
+        int any_abort = 0;
+        for (int r = 0; r < S; ++r) any_abort |= abort_in[r];
         const int n_lo = split * nper;
         const int width = min(128, n_lo + nper) - n_lo;
-        if (width > 0) {
+        if (width > 0 && !any_abort) {
             const int cnt = width * p.M;
             for (int idx = threadIdx.x; idx < cnt; idx += kThreads) {
                 const int m = idx / width;
@@ -389,6 +402,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             mbar_wait(full + (i % kRing), (i / kRing) & 1, &g_fused_error, kErrWaitDrain);
     }
     if (warp == 1) {
+        // every stage warp arrives on accf once all of its MMAs and scale copies
+        // have completed (at once when the epilogue already saw it)
+        if (lane == 0) mbar_wait(accf, 0, &g_fused_error, kErrWaitDrain);
+        __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, Cfg::TMEM_COLS);
     }
@@ -400,15 +417,9 @@ cudaError_t launch_fused_t(const CUtensorMap &tmw, const FusedArgs &args, int n_
 {
     using Cfg = FusedCfg<MMA_N, NV>;
     auto kern = fused_quant_gemm_kernel<MMA_N, NV>;
-    static uint64_t configured = 0;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static KernelOnce once;
+    const cudaError_t e = prepare_kernel(kern, Cfg::SMEM_BYTES, once, nullptr);
     if (e != cudaSuccess) return e;
-    if (!(configured & (1ull << (dev & 63)))) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        configured |= 1ull << (dev & 63);
-    }
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(n_tiles, splits, 1);
@@ -424,7 +435,9 @@ cudaError_t launch_fused_t(const CUtensorMap &tmw, const FusedArgs &args, int n_
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kern, tmw, args);
+    FusedArgs a = args;
+    a.wait_ns = wait_limit_ns();
+    return cudaLaunchKernelEx(&cfg, kern, tmw, a);
 }
 
 }  // namespace

@@ -93,7 +93,8 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
     uint64_t *sf_data = sf_full + STAGES; // [STAGES] the stage's scale bytes are in smem
     uint64_t *accf = sf_data + STAGES;    // a unit's accumulator is complete
     uint64_t *acc_empty = accf + 1;       // the epilogue has drained the accumulator
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 1);
+    uint64_t *cp_done = acc_empty + 1;    // [2] every scale copy of warp 2 / 3 has completed
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(cp_done + 2);
     int *last_flag = reinterpret_cast<int *>(tmem_slot + 1);
     volatile int *abort_flag = last_flag + 1;
     volatile int *epi_go = last_flag + 2;   // [2] per-unit decision of the epilogue warps
@@ -112,6 +113,8 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
         }
         mbar_init(accf, 1);
         mbar_init(acc_empty, 128);
+        mbar_init(cp_done, 1);
+        mbar_init(cp_done + 1, 1);
         *abort_flag = 0;
         fence_mbar_init();
         for (int g = 0; g < p.num_groups; ++g) {
@@ -149,7 +152,7 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
                 for (int i = 0; i < w.nst; ++i, ++gs) {
                     const int slot = gs % STAGES;
                     if (gs >= STAGES &&
-                        !mbar_wait(empty + slot, ((gs / STAGES) - 1) & 1, &g_gemm_error, kErrWaitEmpty)) {
+                        !mbar_wait(empty + slot, ((gs / STAGES) - 1) & 1, &g_gemm_error, kErrWaitEmpty, p.wait_ns)) {
                         *abort_flag = 1;
                         break;
                     }
@@ -185,7 +188,7 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
                 const Unit w = decode_unit(p, u);
                 const GemmProblemDev &pr = p.prob[w.g];
                 const int k_steps_total = (pr.k + 63) / 64;
-                if (ul > 0 && !mbar_wait(acc_empty, (ul - 1) & 1, &g_gemm_error, kErrWaitAccum)) {
+                if (ul > 0 && !mbar_wait(acc_empty, (ul - 1) & 1, &g_gemm_error, kErrWaitAccum, p.wait_ns)) {
                     *abort_flag = 1;
                     break;
                 }
@@ -196,7 +199,7 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
                     const uint32_t ph = (gs / STAGES) & 1;
                     // one wait per stage: the scale-copy threads commit sf_full only
                     // after they also saw the stage's operand tiles land
-                    if (!mbar_wait(sf_full + slot, ph, &g_gemm_error, kErrWaitFull)) {
+                    if (!mbar_wait(sf_full + slot, ph, &g_gemm_error, kErrWaitFull, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -253,14 +256,15 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
             // the MMAs' "empty" commit, so the scale-data wait below orders the
             // copies.
             int gs = 0;
-            for (int u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
+            bool stop = false;
+            for (int u = blockIdx.x; u < units && !stop && !*abort_flag; u += gridDim.x) {
                 const Unit w = decode_unit(p, u);
                 const GemmProblemDev &pr = p.prob[w.g];
                 const int k_steps_total = (pr.k + 63) / 64;
                 for (int i = 0; i < w.nst; ++i, ++gs) {
                     const int slot = gs % STAGES;
-                    if (!mbar_wait(sf_data + slot, (gs / STAGES) & 1, &g_gemm_error, kErrWaitFull)) {
-                        *abort_flag = 1;
+                    if (!mbar_wait(sf_data + slot, (gs / STAGES) & 1, &g_gemm_error, kErrWaitFull, p.wait_ns)) {
+                        stop = true;
                         break;
                     }
                     tc_fence_after();
@@ -281,16 +285,18 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
                     }
                     // the MMA issuer waits only for sf_full: it also stands for the
                     // stage's operand tiles
-                    if (!mbar_wait(full + slot, (gs / STAGES) & 1, &g_gemm_error, kErrWaitFull)) {
-                        *abort_flag = 1;
+                    if (!mbar_wait(full + slot, (gs / STAGES) & 1, &g_gemm_error, kErrWaitFull, p.wait_ns)) {
+                        stop = true;
                         break;
                     }
                     tc_commit(sf_full + slot);
                 }
             }
-            // scale copies still in flight (only after an abort) finish before TMEM is released
-            for (int i = max(0, gs - STAGES); i < gs; ++i)
-                mbar_wait(sf_full + (i % STAGES), (i / STAGES) & 1, &g_gemm_error, kErrWaitDrain);
+            if (stop) *abort_flag = 1;
+            // every scale copy this thread issued (also those of a stage given up
+            // above) completes before TMEM is released
+            tc_commit(cp_done + (warp - 2));
+            mbar_wait(cp_done + (warp - 2), 0, &g_gemm_error, kErrWaitDrain);
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ epilogue
@@ -304,7 +310,7 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
             // one thread waits and decides for all four warps, so that they
             // leave the loop together (the split-K path has named barriers)
             if (threadIdx.x == 128) {
-                const bool ok = mbar_wait(accf, ul & 1, &g_gemm_error, kErrWaitAccum);
+                const bool ok = mbar_wait(accf, ul & 1, &g_gemm_error, kErrWaitAccum, p.wait_ns);
                 if (!ok) *abort_flag = 1;
                 epi_go[ul & 1] = ok;
             }
@@ -380,11 +386,14 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
                 __threadfence();
                 epilogue_bar();
                 if (threadIdx.x == 128) {
-                    const int old = atomicAdd(p.tickets + w.tile, 1);
-                    *last_flag = (old == p.splits - 1);
+                    // a split that gave up adds 2^20 as well: the last split then
+                    // leaves C unwritten instead of summing missing partials
+                    const int old = atomicAdd(p.tickets + w.tile, run ? 1 : 1 + (1 << 20));
+                    const bool last = (old & 0xFFFFF) == p.splits - 1;
+                    *last_flag = !last ? 0 : ((old >> 20) == 0 && run) ? 1 : 2;
                 }
                 epilogue_bar();
-                if (run && *last_flag) {
+                if (*last_flag == 1) {
                     __threadfence();
                     for (int c0 = 0; c0 < BN; c0 += 32) {
                         const int col0 = w.n_tile * BN + c0;
@@ -406,8 +415,9 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
                         for (int j = 0; j < 16; ++j) pk[j] = pack2<F16>(f[2 * j], f[2 * j + 1]);
                         store_packed32(pr.c, pr.ldc, row, col0, pr.n, pk);
                     }
-                    if (threadIdx.x == 128) p.tickets[w.tile] = 0;
                 }
+                // the last split leaves its ticket at zero, also after an abort
+                if (threadIdx.x == 128 && *last_flag) p.tickets[w.tile] = 0;
                 epilogue_bar();   // last_flag is reused by the next unit
             }
         }
@@ -435,20 +445,12 @@ cudaError_t launch_bs_gemm(const GemmParams<MAXG> &params, cudaStream_t stream)
 {
     using Cfg = GemmCfg<KIND, BN, STAGES>;
     auto kern = bs_gemm_kernel<KIND, BN, STAGES, MAXG, F16, EPI>;
-    static uint64_t configured = 0;  // one bit per device; setting it twice is harmless
-    static int sms_of[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static KernelOnce once;
+    int sms = 0;
+    const cudaError_t e = prepare_kernel(kern, Cfg::SMEM_BYTES, once, &sms);
     if (e != cudaSuccess) return e;
-    if (!(configured & (1ull << (dev & 63)))) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        e = cudaDeviceGetAttribute(&sms_of[dev & 63], cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        configured |= 1ull << (dev & 63);
-    }
     const int units = params.total_tiles * params.splits;
-    const int grid = min(units, max(1, sms_of[dev & 63]));
+    const int grid = min(units, max(1, sms));
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(grid, 1, 1);
@@ -460,7 +462,9 @@ cudaError_t launch_bs_gemm(const GemmParams<MAXG> &params, cudaStream_t stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, params);
+    GemmParams<MAXG> P = params;
+    P.wait_ns = wait_limit_ns();
+    return cudaLaunchKernelEx(&cfg, kern, P);
 }
 
 constexpr int kMxStages = 4;        // BN = 256

@@ -35,6 +35,7 @@ struct GemmParams {
     int pad_;
     float *partials;
     int *tickets;
+    uint64_t wait_ns;   // limit of the waits that guard work
 };
 
 __host__ __device__ constexpr uint32_t pow2_cols(uint32_t n)
@@ -56,13 +57,14 @@ struct GemmCfg {
     static constexpr uint32_t SF_COLS_B = NCH * SF_BLK * 4;
     static constexpr uint32_t SF_COLS = SF_COLS_A + SF_COLS_B;
     static constexpr uint32_t TMEM_COLS = pow2_cols(BN + STAGES * SF_COLS);
-    static constexpr uint32_t BAR_BYTES = 256;
+    static constexpr uint32_t BAR_BYTES = 512;
     static constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
     static_assert(STAGE_BYTES % 1024 == 0, "stage must keep 1024-byte alignment");
     static_assert(BN + STAGES * SF_COLS <= 512, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-    // full, empty, sf_full, sf_data per stage; accf, acc_empty; TMEM address and flags
-    static_assert((4 * STAGES + 2) * 8 + 16 <= BAR_BYTES, "barrier area");
+    // full, empty, sf_full, sf_data per stage; accf, acc_empty, two drain
+    // barriers; TMEM address and flags
+    static_assert((4 * STAGES + 4) * 8 + 16 <= BAR_BYTES, "barrier area");
 };
 
 template <bool F16>

@@ -60,8 +60,9 @@ struct PairCfg {
     static_assert(STAGE_BYTES % 1024 == 0, "stage must keep 1024-byte alignment");
     static_assert(256 + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-    // full, sf_data, empty, sf_full per stage; accf, acc_empty; TMEM address and flags
-    static_assert((4 * STAGES + 2) * 8 + 16 <= BAR_BYTES, "barrier area");
+    // full, sf_data, empty, sf_full per stage; accf, acc_empty, two drain
+    // barriers; TMEM address, flags and the producer's stage count
+    static_assert((4 * STAGES + 4) * 8 + 24 <= BAR_BYTES, "barrier area");
 };
 
 __device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -75,6 +76,7 @@ struct PairParams {
     GemmProblemDev prob[MAXG];
     int num_groups;
     int total_tiles;
+    uint64_t wait_ns;          // limit of the waits that guard work
 };
 
 struct PairUnit {
@@ -111,9 +113,11 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_pair_kernel(const __grid_const
     uint64_t *sf_full = empty + STAGES;     // rank 0: the stage's scales are in both TMEMs
     uint64_t *accf = sf_full + STAGES;      // the tile's accumulator is complete
     uint64_t *acc_empty = accf + 1;         // rank 0: both CTAs' epilogues drained it
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 1);
+    uint64_t *cp_done = acc_empty + 1;      // [2] rank 0: every scale copy of warp 2 / 3 completed
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(cp_done + 2);
     volatile int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
     volatile int *epi_go = abort_flag + 1;  // [2] per-tile decision of the epilogue warps
+    volatile int *issued_slot = epi_go + 2; // stages this CTA's producer issued (read by rank 0 at exit)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -133,6 +137,8 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_pair_kernel(const __grid_const
         }
         mbar_init(accf, 1);
         mbar_init(acc_empty, 8);         // one arrival per epilogue warp of each CTA
+        mbar_init(cp_done, 1);
+        mbar_init(cp_done + 1, 1);
         *abort_flag = 0;
         fence_mbar_init();
         for (int g = 0; g < p.num_groups; ++g) {
@@ -178,8 +184,8 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_pair_kernel(const __grid_const
                 const int k_stages = (pr.k + 255) / 256;
                 for (int i = 0; i < k_stages; ++i, ++gs) {
                     const int slot = gs % STAGES;
-                    if (gs >= STAGES &&
-                        !mbar_wait(empty + slot, ((gs / STAGES) - 1) & 1, &g_gemm_pair_error, kErrWaitEmpty)) {
+                    if (gs >= STAGES && !mbar_wait(empty + slot, ((gs / STAGES) - 1) & 1, &g_gemm_pair_error,
+                                                   kErrWaitEmpty, p.wait_ns)) {
                         *abort_flag = 1;
                         break;
                     }
@@ -214,7 +220,8 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_pair_kernel(const __grid_const
                 const GemmProblemDev &pr = p.prob[w.g];
                 const int k_stages = (pr.k + 255) / 256;
                 const int k_steps_total = (pr.k + 63) / 64;
-                if (ul > 0 && !mbar_wait<true>(acc_empty, (ul - 1) & 1, &g_gemm_pair_error, kErrWaitAccum)) {
+                if (ul > 0 &&
+                    !mbar_wait<true>(acc_empty, (ul - 1) & 1, &g_gemm_pair_error, kErrWaitAccum, p.wait_ns)) {
                     *abort_flag = 1;
                     break;
                 }
@@ -225,7 +232,7 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_pair_kernel(const __grid_const
                     const uint32_t ph = (gs / STAGES) & 1;
                     // one wait per stage: the scale-copy threads commit sf_full only
                     // after they also saw the stage's operand tiles land
-                    if (!mbar_wait(sf_full + slot, ph, &g_gemm_pair_error, kErrWaitFull)) {
+                    if (!mbar_wait(sf_full + slot, ph, &g_gemm_pair_error, kErrWaitFull, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -278,7 +285,8 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_pair_kernel(const __grid_const
             // half past N, K blocks past K) arrive as zeros and feed only
             // accumulator rows and columns that are never stored.
             int gs = 0;
-            for (int u = pair; u < units && !*abort_flag; u += npairs) {
+            bool stop = false;
+            for (int u = pair; u < units && !stop && !*abort_flag; u += npairs) {
                 const PairUnit w = decode_pair_unit(p, u);
                 const GemmProblemDev &pr = p.prob[w.g];
                 const int k_stages = (pr.k + 255) / 256;
@@ -286,8 +294,8 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_pair_kernel(const __grid_const
                 for (int i = 0; i < k_stages; ++i, ++gs) {
                     const int slot = gs % STAGES;
                     const uint32_t ph = (gs / STAGES) & 1;
-                    if (!mbar_wait(sf_data + slot, ph, &g_gemm_pair_error, kErrWaitFull)) {
-                        *abort_flag = 1;
+                    if (!mbar_wait(sf_data + slot, ph, &g_gemm_pair_error, kErrWaitFull, p.wait_ns)) {
+                        stop = true;
                         break;
                     }
                     tc_fence_after();
@@ -306,16 +314,18 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_pair_kernel(const __grid_const
                     }
                     // the MMA issuer waits only for sf_full: it also stands for the
                     // stage's operand tiles
-                    if (!mbar_wait(full + slot, ph, &g_gemm_pair_error, kErrWaitFull)) {
-                        *abort_flag = 1;
+                    if (!mbar_wait(full + slot, ph, &g_gemm_pair_error, kErrWaitFull, p.wait_ns)) {
+                        stop = true;
                         break;
                     }
                     tc_commit_pair(sf_full + slot);
                 }
             }
-            // copies still in flight (only after an abort) finish before TMEM is freed
-            for (int i = max(0, gs - STAGES); i < gs; ++i)
-                mbar_wait(sf_full + (i % STAGES), (i / STAGES) & 1, &g_gemm_pair_error, kErrWaitDrain);
+            if (stop) *abort_flag = 1;
+            // every scale copy this thread issued (also those of a stage given up
+            // above) completes before the pair frees TMEM
+            tc_commit_pair(cp_done + (warp - 2));
+            mbar_wait(cp_done + (warp - 2), 0, &g_gemm_pair_error, kErrWaitDrain);
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ epilogue
@@ -330,7 +340,7 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_pair_kernel(const __grid_const
             // one thread waits and decides for the four warps, so that they
             // leave the loop together
             if (threadIdx.x == 128) {
-                const bool ok = mbar_wait(accf, ul & 1, &g_gemm_pair_error, kErrWaitAccum);
+                const bool ok = mbar_wait(accf, ul & 1, &g_gemm_pair_error, kErrWaitAccum, p.wait_ns);
                 if (!ok) *abort_flag = 1;
                 epi_go[ul & 1] = ok;
             }
@@ -395,11 +405,32 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_pair_kernel(const __grid_const
     __syncwarp();
 
     // ----------------------------------------------------------- teardown
+    // Copies still in flight (only after an abort) must land before either CTA
+    // leaves. Rank 0's barriers count both CTAs' copies, and after an abort the
+    // two producers may have issued different numbers of stages: rank 0 reads
+    // rank 1's count, settles the share of each stage that only one CTA issued
+    // (arms the phase with rank 1's bytes, or cancels rank 1's missing bytes),
+    // then waits for every stage that can still be in flight.
     tc_fence_before();
+    if (warp == 0 && lane == 0) *issued_slot = issued;
+    cluster_sync();
     if (warp == 0 && lane == 0 && leader) {
-        // copies still in flight (only after an abort) must land before exit;
-        // rank 0's barriers count both CTAs' copies
-        for (int i = max(0, issued - STAGES); i < issued; ++i) {
+        const int i0 = issued;
+        const int i1 = static_cast<int>(ld_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int *>(issued_slot)), 1)));
+        const int hi = max(i0, i1);
+        constexpr uint32_t kSfOne = Cfg::SFA_BYTES + Cfg::SFB_BYTES;   // one CTA's bytes of a stage
+        constexpr uint32_t kOpOne = Cfg::A_BYTES + Cfg::B_BYTES;
+        for (int i = min(i0, i1); i < hi; ++i) {
+            const int slot = i % STAGES;
+            if (i >= i0) {
+                mbar_arrive_expect_tx(sf_data + slot, kSfOne);
+                mbar_arrive_expect_tx(full + slot, kOpOne);
+            } else {
+                mbar_complete_tx(sf_data + slot, kSfOne);
+                mbar_complete_tx(full + slot, kOpOne);
+            }
+        }
+        for (int i = max(0, hi - STAGES); i < hi; ++i) {
             mbar_wait(sf_data + (i % STAGES), (i / STAGES) & 1, &g_gemm_pair_error, kErrWaitDrain);
             mbar_wait(full + (i % STAGES), (i / STAGES) & 1, &g_gemm_pair_error, kErrWaitDrain);
         }
@@ -418,19 +449,11 @@ cudaError_t launch_pair(const PairParams<MAXG> &params, cudaStream_t stream)
 {
     using Cfg = PairCfg<KIND, STAGES>;
     auto kern = bs_gemm_pair_kernel<KIND, STAGES, MAXG, F16, EPI>;
-    static uint64_t configured = 0;  // one bit per device; setting it twice is harmless
-    static int sms_of[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static KernelOnce once;
+    int sms = 0;
+    const cudaError_t e = prepare_kernel(kern, Cfg::SMEM_BYTES, once, &sms);
     if (e != cudaSuccess) return e;
-    if (!(configured & (1ull << (dev & 63)))) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        e = cudaDeviceGetAttribute(&sms_of[dev & 63], cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        configured |= 1ull << (dev & 63);
-    }
-    const int pairs = min(params.total_tiles, max(1, sms_of[dev & 63] / 2));
+    const int pairs = min(params.total_tiles, max(1, sms / 2));
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(2 * pairs, 1, 1);
@@ -446,7 +469,9 @@ cudaError_t launch_pair(const PairParams<MAXG> &params, cudaStream_t stream)
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kern, params);
+    PairParams<MAXG> P = params;
+    P.wait_ns = wait_limit_ns();
+    return cudaLaunchKernelEx(&cfg, kern, P);
 }
 
 constexpr int kPairMxStages = 6;   // 35 KB stages

@@ -6,9 +6,50 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace mxfp4 {
 
 constexpr int kMaxGroups = 16;
+
+// Default limit of every bounded wait in the kernels (2 s of %globaltimer).
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+
+// Limit of the waits that guard work in kernels launched from now on
+// (mxfp4_set_wait_limit_ns); the waits on a kernel's exit path keep the
+// default. Process-wide, read at every launch.
+uint64_t wait_limit_ns();
+void set_wait_limit_ns(uint64_t ns);
+
+// Per-device, set-once facts of one kernel instantiation: its dynamic
+// shared-memory limit is raised once per device and the device's SM count is
+// read once. Safe when launches come from several host threads (at worst two
+// threads both set the same attribute).
+struct KernelOnce {
+    std::atomic<uint64_t> done{0};
+    std::atomic<int> sms[64];
+};
+
+template <typename Kern>
+cudaError_t prepare_kernel(Kern kern, uint32_t smem_bytes, KernelOnce &once, int *sms)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    const uint64_t bit = 1ull << dev;
+    if (!(once.done.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes));
+        if (e != cudaSuccess) return e;
+        int n = 0;
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        once.sms[dev].store(n, std::memory_order_relaxed);
+        once.done.fetch_or(bit, std::memory_order_release);
+    }
+    if (sms) *sms = once.sms[dev].load(std::memory_order_relaxed);
+    return cudaSuccess;
+}
 
 // ---------------------------------------------------------------- quant.cu
 cudaError_t launch_quant_mx(const void *A, int64_t M, int64_t K, int64_t lda, void *Aq,

@@ -7,6 +7,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "internal.h"
+
 namespace mxfp4 {
 
 // Device-side error codes recorded by bounded waits (0 = none).
@@ -20,8 +22,10 @@ enum DeviceError : int {
     kErrWaitPeer = 6,     // waited too long for the other CTA of a pair
 };
 
-// A wait gives up after this many nanoseconds of %globaltimer.
-constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+// Waits that guard work give up after the limit the launch passes (the
+// kWaitTimeoutNs default unless the host set another); the waits of a
+// kernel's exit path, which must see every copy and MMA it issued land before
+// it frees shared memory and TMEM, always use the default.
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
@@ -87,19 +91,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 }
 
 // Waits for the phase with the given parity to complete. Returns false after
-// kWaitTimeoutNs, having recorded `code` in *err (first error wins).
+// limit_ns nanoseconds, having recorded `code` in *err (first error wins).
 template <bool CLUSTER = false>
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err, int code)
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err, int code,
+                                          uint64_t limit_ns = kWaitTimeoutNs)
 {
     if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
         if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
-        if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+        if (global_timer_ns() - t0 > limit_ns) {
             atomicCAS(err, 0, code);
             return false;
         }
     }
+}
+
+// Lowers the transaction count of the current phase of `bar` by `bytes`, as
+// if that many bytes of an expected copy had landed.
+__device__ __forceinline__ void mbar_complete_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
 // Arrive on an mbarrier of a CTA of this cluster (address from mapa_shared);
@@ -432,6 +444,18 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank)
 __device__ __forceinline__ void st_shared_cluster_f32(uint32_t addr, float v)
 {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
 }
 
 // ------------------------------------------------------------ FP4 encoding

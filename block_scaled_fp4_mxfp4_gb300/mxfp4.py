@@ -102,6 +102,8 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.mxfp4_gemm_a4w4_noalloc.argtypes = [_p, _i64, _p, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p]
     L.mxfp4_get_device_error.restype = _st
     L.mxfp4_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    L.mxfp4_set_wait_limit_ns.restype = ctypes.c_uint64
+    L.mxfp4_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     L.mxfp4_gemm_plan.restype = _st
     L.mxfp4_gemm_plan.argtypes = [_i64, _i64, _i64, ctypes.c_int, ctypes.POINTER(Plan)]
     L.nvfp4_group_gemm_plan.restype = _st
@@ -404,6 +406,12 @@ def nvfp4_group_gemm_plan(problems) -> dict:
     p = Plan()
     _check(lib().nvfp4_group_gemm_plan(problems, len(problems), ctypes.byref(p)), "nvfp4_group_gemm_plan")
     return _plan_dict(p)
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    """Limit of the kernels' work-guarding waits for later launches (0: the
+    default of 2 s); returns the previous limit."""
+    return int(_lib.mxfp4_set_wait_limit_ns(int(ns)))
 
 
 def get_device_error() -> int:

@@ -206,7 +206,7 @@ def gen_a(w: MXWorkload, M: int = None) -> np.ndarray:
     else:
         x = normal(key, n, w.a_sigma)
     if w.a_dist == "heavy":
-        x = _heavy_tail(w, x.reshape(w.M, w.K)[:M]).ravel()
+        x = _heavy_tail(w, x.reshape(M, w.K)).ravel()
     return to_bf16_bits(x).reshape(M, w.K)
 
 

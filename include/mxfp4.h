@@ -351,10 +351,28 @@ MXFP4_API mxfp4_status_t mxfp4_group_gemm_plan(const mxfp4_problem_t *problems, 
                                                mxfp4_plan_t *out);
 
 /* Reads and clears the library's device-side error word. Kernels never trap:
- * a wait that exceeds its time limit (about 2 s) records a nonzero code there
- * and the kernel exits cleanly. This call synchronizes the current device.
- * *code receives 0 when no kernel reported an error. */
+ * a wait that exceeds its time limit (2 s unless mxfp4_set_wait_limit_ns set
+ * another) records a nonzero code there and the kernel exits cleanly, after
+ * every copy and MMA it issued has landed and with its TMEM freed. Because
+ * the launching call has already returned MXFP4_OK by then, this is the only
+ * place such a failure shows: a call whose kernel gave up leaves its outputs
+ * unspecified (the GEMM kernels skip the stores of every tile, or K-split,
+ * whose inputs did not all arrive, rather than store partial sums) and may
+ * leave the split-K counters of its workspace nonzero, so clear the
+ * workspace before reusing it after a nonzero code. This call synchronizes
+ * the current device. *code receives 0 when no kernel reported an error;
+ * otherwise 1..15 (single-CTA GEMM), 16 + c (fused kernel) or 32 + c
+ * (CTA-pair GEMM), c naming the wait that gave up. */
 MXFP4_API mxfp4_status_t mxfp4_get_device_error(int *code);
+
+/* Sets the time limit, in nanoseconds, of the waits that guard work inside
+ * every kernel launched afterwards (process-wide; 0 restores the default of
+ * 2 s) and returns the previous limit. The waits on a kernel's exit path,
+ * which keep shared memory and TMEM alive until every copy and MMA the kernel
+ * issued has landed, always keep 2 s. A short limit makes the kernels give up
+ * on their own: tests use it to exercise the error path without faulting the
+ * GPU. Not meant for production use. */
+MXFP4_API uint64_t mxfp4_set_wait_limit_ns(uint64_t ns);
 
 #ifdef __cplusplus
 }

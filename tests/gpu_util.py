@@ -45,6 +45,22 @@ def assert_within_tolerance(c_gpu: np.ndarray, c_ref: np.ndarray, s_abs: np.ndar
     return worst
 
 
+def gemm_sampled_parallel(qa, sfa, qb, sfb, K: int, vec: int, rows, cols, threads: int = 0):
+    """oracle.gemm_sampled over host threads (the oracle's C loop releases the
+    GIL; every output is computed by the same definition, so the split changes
+    nothing but the wall time)."""
+    import concurrent.futures as cf
+    import os
+    threads = threads or max(1, min(32, len(os.sched_getaffinity(0))))
+    n = len(rows)
+    edges = [n * i // threads for i in range(threads + 1)]
+    parts = [(edges[i], edges[i + 1]) for i in range(threads) if edges[i + 1] > edges[i]]
+    with cf.ThreadPoolExecutor(max_workers=len(parts)) as ex:
+        res = list(ex.map(lambda lh: oracle.gemm_sampled(qa, sfa, qb, sfb, K, vec, rows[lh[0]:lh[1]],
+                                                          cols[lh[0]:lh[1]]), parts))
+    return np.concatenate([r[0] for r in res]), np.concatenate([r[1] for r in res])
+
+
 def sample_pairs(M: int, N: int, n_random: int, n_rows: int, n_cols: int, seed: int):
     """Random (m, n) pairs plus a few full rows and full columns."""
     from block_scaled_fp4_mxfp4_gb300 import workloads as wl

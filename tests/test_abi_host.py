@@ -14,9 +14,16 @@ L = mxfp4.lib()
 
 def test_every_declared_symbol_is_exported():
     names = mxfp4.declared_symbols()
-    assert len(names) == 22
+    assert len(names) == 23
     for n in names:
         assert hasattr(L, n), n  # ctypes resolves the exported symbol
+
+
+def test_wait_limit_setter_returns_previous_and_zero_restores_default():
+    default = 2_000_000_000
+    assert mxfp4.set_wait_limit_ns(1234) == default
+    assert mxfp4.set_wait_limit_ns(0) == 1234
+    assert mxfp4.set_wait_limit_ns(0) == default
 
 
 def test_status_strings_and_version():

@@ -11,7 +11,8 @@ import torch
 
 import oracle
 from block_scaled_fp4_mxfp4_gb300 import workloads as wl
-from gpu_util import assert_bytes_equal, assert_within_tolerance, c_f64, dev_bf16, host, sample_pairs
+from gpu_util import (assert_bytes_equal, assert_within_tolerance, c_f64, dev_bf16, gemm_sampled_parallel, host,
+                      sample_pairs)
 
 pytestmark = pytest.mark.gpu
 
@@ -38,7 +39,7 @@ def run_mx_workload(w, sampled):
         assert_within_tolerance(c_f64(C), c_ref, s, w.name)
     else:
         rows, cols = sample_pairs(w.M, w.N, *sampled, seed=17)
-        c_ref, s = oracle.gemm_sampled(qa_r, sfa_r, qb_r, sfb_r, w.K, 32, rows, cols)
+        c_ref, s = gemm_sampled_parallel(qa_r, sfa_r, qb_r, sfb_r, w.K, 32, rows, cols)
         got = C[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].float().cpu().numpy()
         assert_within_tolerance(got.astype(np.float64), c_ref, s, w.name + " (sampled)")
     assert mx.get_device_error() == 0
@@ -57,7 +58,8 @@ def test_medium_heavy_tail_sampled():
 
 
 def test_compute_8192_sampled():
-    run_mx_workload(wl.COMPUTE, (4096, 2, 2))
+    # 65,536 random outputs plus 16 whole rows and 16 whole columns
+    run_mx_workload(wl.COMPUTE, (65536, 16, 16))
 
 
 def test_nvfp4_grouped_sampled():
