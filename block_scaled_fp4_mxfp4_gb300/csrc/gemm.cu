@@ -177,84 +177,81 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
                 }
             }
         }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            // -------------------------------------------------------- MMA issuer
-            // Only MMAs are issued here (a tcgen05 instruction costs tens of
-            // cycles to issue); warps 2 and 3 stage the scale factors into TMEM.
-            constexpr uint32_t IDESC = idesc_block_scaled(BN, MX);
-            int gs = 0, ul = 0, commits = 0;
-            for (int u = blockIdx.x; u < units; u += gridDim.x, ++ul) {
-                const Unit w = decode_unit(p, u);
-                const GemmProblemDev &pr = p.prob[w.g];
-                const int k_steps_total = (pr.k + 63) / 64;
-                if (ul > 0 && !mbar_wait(acc_empty, (ul - 1) & 1, &g_gemm_error, kErrWaitAccum, p.wait_ns)) {
-                    *abort_flag = 1;
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        // Only MMAs are issued here (a tcgen05 instruction costs tens of cycles
+        // to issue); warps 2 and 3 stage the scale factors into TMEM.
+        constexpr uint32_t IDESC = idesc_block_scaled(BN, MX);
+        int gs = 0, ul = 0, commits = 0;
+        for (int u = blockIdx.x; u < units; u += gridDim.x, ++ul) {
+            const Unit w = decode_unit(p, u);
+            const GemmProblemDev &pr = p.prob[w.g];
+            const int k_steps_total = (pr.k + 63) / 64;
+            if (ul > 0 && !mbar_wait(acc_empty, (ul - 1) & 1, &g_gemm_error, kErrWaitAccum, p.wait_ns)) {
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            bool ok = true;
+            for (int i = 0; i < w.nst; ++i, ++gs) {
+                const int slot = gs % STAGES;
+                const uint32_t ph = (gs / STAGES) & 1;
+                // one wait per stage: the scale-copy threads commit sf_full only
+                // after they also saw the stage's operand tiles land
+                if (!mbar_wait(sf_full + slot, ph, &g_gemm_error, kErrWaitFull, p.wait_ns)) {
+                    ok = false;
                     break;
                 }
                 tc_fence_after();
-                bool ok = true;
-                for (int i = 0; i < w.nst; ++i, ++gs) {
-                    const int slot = gs % STAGES;
-                    const uint32_t ph = (gs / STAGES) & 1;
-                    // one wait per stage: the scale-copy threads commit sf_full only
-                    // after they also saw the stage's operand tiles land
-                    if (!mbar_wait(sf_full + slot, ph, &g_gemm_error, kErrWaitFull, p.wait_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
-                    const uint32_t a_base = smem_u32(st);
-                    const uint32_t b_base = smem_u32(st + Cfg::A_BYTES);
-                    const uint32_t tsfa = tmem_sf + slot * Cfg::SF_COLS;
-                    const uint32_t tsfb = tsfa + Cfg::SF_COLS_A;
-                    const int ks = w.s_begin + i;
-                    // K step kk of the stage starts 32 bytes (2 descriptor units) further
-                    const uint64_t ad = sdesc_sw128(a_base);
-                    const uint64_t bd = sdesc_sw128(b_base);
-                    const int ksteps = min(4, k_steps_total - ks * 4);
-                    auto mma_step = [&](int kk) {
-                        const int blk = MX ? kk / 2 : kk;
-                        const uint32_t sfid = MX ? static_cast<uint32_t>(kk & 1) * 2u : 0u;
-                        const uint32_t idesc = idesc_with_sf_ids(IDESC, sfid, sfid);
-                        const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-                        if constexpr (MX)
-                            mma_mxf4(tmem_acc, ad + 2 * kk, bd + 2 * kk, idesc, tsfa + blk * 4, tsfb + blk * Cfg::NCH * 4, acc);
-                        else
-                            mma_nvf4(tmem_acc, ad + 2 * kk, bd + 2 * kk, idesc, tsfa + blk * 4, tsfb + blk * Cfg::NCH * 4, acc);
-                    };
-                    // the issuing thread is the bottleneck: full stages go unrolled
-                    if (ksteps == 4) {
+                uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
+                const uint32_t a_base = smem_u32(st);
+                const uint32_t b_base = smem_u32(st + Cfg::A_BYTES);
+                const uint32_t tsfa = tmem_sf + slot * Cfg::SF_COLS;
+                const uint32_t tsfb = tsfa + Cfg::SF_COLS_A;
+                const int ks = w.s_begin + i;
+                // K step kk of the stage starts 32 bytes (2 descriptor units) further
+                const uint64_t ad = sdesc_sw128(a_base);
+                const uint64_t bd = sdesc_sw128(b_base);
+                const int ksteps = min(4, k_steps_total - ks * 4);
+                auto mma_step = [&](int kk) {
+                    const int blk = MX ? kk / 2 : kk;
+                    const uint32_t sfid = MX ? static_cast<uint32_t>(kk & 1) * 2u : 0u;
+                    const uint32_t idesc = idesc_with_sf_ids(IDESC, sfid, sfid);
+                    const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                    if constexpr (MX)
+                        mma_mxf4(tmem_acc, ad + 2 * kk, bd + 2 * kk, idesc, tsfa + blk * 4, tsfb + blk * Cfg::NCH * 4, acc);
+                    else
+                        mma_nvf4(tmem_acc, ad + 2 * kk, bd + 2 * kk, idesc, tsfa + blk * 4, tsfb + blk * Cfg::NCH * 4, acc);
+                };
+                // the issuing thread is the bottleneck: full stages go unrolled
+                if (ksteps == 4) {
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) mma_step(kk);
-                    } else {
-                        for (int kk = 0; kk < ksteps; ++kk) mma_step(kk);
-                    }
-                    tc_commit(empty + slot);
+                    for (int kk = 0; kk < 4; ++kk) mma_step(kk);
+                } else {
+                    for (int kk = 0; kk < ksteps; ++kk) mma_step(kk);
                 }
-                // arrives once every MMA issued above has completed (also on abort)
-                tc_commit(accf);
-                ++commits;
-                if (!ok) {
-                    *abort_flag = 1;
-                    break;
-                }
+                tc_commit(empty + slot);
             }
-            // The epilogue waits for every commit unless it stopped early; the
-            // accumulator must not be in use when TMEM is released.
-            if (commits > 0) mbar_wait(accf, (commits - 1) & 1, &g_gemm_error, kErrWaitDrain);
+            // arrives once every MMA issued above has completed (also on abort)
+            tc_commit(accf);
+            ++commits;
+            if (!ok) {
+                *abort_flag = 1;
+                break;
+            }
         }
+        // The epilogue waits for every commit unless it stopped early; the
+        // accumulator must not be in use when TMEM is released.
+        if (commits > 0) mbar_wait(accf, (commits - 1) & 1, &g_gemm_error, kErrWaitDrain);
     } else if (warp == 2 || warp == 3) {
         if (lane == 0) {
             // ----------------------------------------- scale staging, smem -> TMEM
             // Lane 0 of warps 2 and 3 share the copies of each stage (even and odd
             // K blocks): one tcgen05.cp takes tens of cycles to issue, and a
-            // stage of NVFP4 scales needs twelve.
-            // A stage's TMEM scale slot is rewritten only after the stage that
-            // used it has been consumed: its smem slot was refilled, which needed
-            // the MMAs' "empty" commit, so the scale-data wait below orders the
-            // copies.
+            // stage of NVFP4 scales needs twelve. A stage's TMEM scale slot is
+            // rewritten only after the stage that used it has been consumed: its
+            // smem slot was refilled, which needed the MMAs' "empty" commit, so
+            // the scale-data wait below orders the copies.
             int gs = 0;
             bool stop = false;
             for (int u = blockIdx.x; u < units && !stop && !*abort_flag; u += gridDim.x) {

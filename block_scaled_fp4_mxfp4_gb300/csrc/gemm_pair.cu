@@ -65,7 +65,10 @@ struct PairCfg {
     static_assert((4 * STAGES + 4) * 8 + 24 <= BAR_BYTES, "barrier area");
 };
 
-__device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+constexpr int kPairThreads = 384;        // warps 0-3: producer, MMA issuer, two scale-copy warps; 4-11: epilogue
+constexpr int kPairEpiWarps = 8;
+
+__device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 template <int MAXG>
 struct PairParams {
@@ -101,7 +104,7 @@ __device__ __forceinline__ PairUnit decode_pair_unit(const PairParams<MAXG> &p, 
 
 // EPI: the variant with the alpha / beta / bias epilogue (mxfp4_gemm_a4w4_ex).
 template <int KIND, int STAGES, int MAXG, bool F16, bool EPI = false>
-__global__ void __launch_bounds__(256, 1) bs_gemm_pair_kernel(const __grid_constant__ PairParams<MAXG> p)
+__global__ void __launch_bounds__(kPairThreads, 1) bs_gemm_pair_kernel(const __grid_constant__ PairParams<MAXG> p)
 {
     using Cfg = PairCfg<KIND, STAGES>;
     constexpr bool MX = Cfg::MX;
@@ -136,7 +139,7 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_pair_kernel(const __grid_const
             mbar_init(sf_full + s, 2);   // one commit from each scale-copy thread
         }
         mbar_init(accf, 1);
-        mbar_init(acc_empty, 8);         // one arrival per epilogue warp of each CTA
+        mbar_init(acc_empty, 2 * kPairEpiWarps);   // one arrival per epilogue warp of each CTA
         mbar_init(cp_done, 1);
         mbar_init(cp_done + 1, 1);
         *abort_flag = 0;
@@ -211,7 +214,7 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_pair_kernel(const __grid_const
             }
         }
     } else if (warp == 1) {
-        if (lane == 0 && leader) {
+        if (leader && lane == 0) {
             // --------------------------------------------- MMA issuer (rank 0)
             constexpr uint32_t IDESC = idesc_block_scaled(256, MX, 256);
             int gs = 0, ul = 0, commits = 0;
@@ -220,8 +223,9 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_pair_kernel(const __grid_const
                 const GemmProblemDev &pr = p.prob[w.g];
                 const int k_stages = (pr.k + 255) / 256;
                 const int k_steps_total = (pr.k + 63) / 64;
-                if (ul > 0 &&
-                    !mbar_wait<true>(acc_empty, (ul - 1) & 1, &g_gemm_pair_error, kErrWaitAccum, p.wait_ns)) {
+                // the epilogues' arrivals are relaxed: they publish no data, only
+                // that their TMEM loads of the accumulator have completed
+                if (ul > 0 && !mbar_wait(acc_empty, (ul - 1) & 1, &g_gemm_pair_error, kErrWaitAccum, p.wait_ns)) {
                     *abort_flag = 1;
                     break;
                 }
@@ -279,10 +283,11 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_pair_kernel(const __grid_const
     } else if (warp == 2 || warp == 3) {
         if (lane == 0 && leader) {
             // ------------------------- scale staging for both CTAs (rank 0)
-            // A stage's TMEM scale slot is rewritten only after both CTAs
-            // refilled the stage's smem, which needed the MMAs' "empty" commit.
-            // Scale blocks past the problem (a second CTA without rows, a B
-            // half past N, K blocks past K) arrive as zeros and feed only
+            // Lane 0 of warps 2 and 3 share the copies of each stage (even / odd
+            // K blocks). A stage's TMEM scale slot is rewritten only after both
+            // CTAs refilled the stage's smem, which needed the MMAs' "empty"
+            // commit. Scale blocks past the problem (a second CTA without rows,
+            // a B half past N, K blocks past K) arrive as zeros and feed only
             // accumulator rows and columns that are never stored.
             int gs = 0;
             bool stop = false;
@@ -329,15 +334,22 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_pair_kernel(const __grid_const
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ epilogue
+        // Eight warps: warp 4 + e reads TMEM lane quadrant e % 4 (the 32 rows
+        // it may access) and columns [128 h, 128 h + 128), h = e / 4. Its two
+        // pairs of 32-column loads are each in flight together, then the warp
+        // hands TMEM back (a relaxed arrive on rank 0's barrier: the MMA
+        // issuer only needs to know that the loads have completed) and stores.
+        const int e = warp - 4;
         const int q = warp & 3;                  // TMEM lane quadrant of this warp
+        const int h = e >> 2;                    // column half
         const int row_in_tile = q * 32 + lane;
-        const uint32_t t_row = tmem_acc + (static_cast<uint32_t>(q * 32) << 16);
+        const uint32_t t_row = tmem_acc + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * 128);
         const uint32_t acc_empty_r0 = mapa_shared(smem_u32(acc_empty), 0);
         int ul = 0;
         for (int u = pair; u < units; u += npairs, ++ul) {
             const PairUnit w = decode_pair_unit(p, u);
             const GemmProblemDev &pr = p.prob[w.g];
-            // one thread waits and decides for the four warps, so that they
+            // one thread waits and decides for the eight warps, so that they
             // leave the loop together
             if (threadIdx.x == 128) {
                 const bool ok = mbar_wait(accf, ul & 1, &g_gemm_pair_error, kErrWaitAccum, p.wait_ns);
@@ -349,15 +361,16 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_pair_kernel(const __grid_const
             tc_fence_after();
             const bool run = (*abort_flag == 0);
             const int row = w.m_pair * 256 + static_cast<int>(rank) * 128 + row_in_tile;
+            const int col_base = w.n_tile * 256 + h * 128;
             if (EPI && pr.epi) {
                 // epilogue with alpha / beta / bias: each 32-column chunk is
                 // finished and stored straight from TMEM, then TMEM goes back
 #pragma unroll 1
-                for (int c = 0; c < 8; ++c) {
+                for (int c = 0; c < 4; ++c) {
                     uint32_t v[32];
                     tmem_ld32(t_row + c * 32, v);
                     tmem_ld_wait();
-                    const int col0 = w.n_tile * 256 + c * 32;
+                    const int col0 = col_base + c * 32;
                     if (run && row < pr.m && col0 < pr.n) {
                         uint32_t part[16];
 #pragma unroll
@@ -371,27 +384,31 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_pair_kernel(const __grid_const
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(acc_empty_r0);
+                if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty_r0);
                 continue;
             }
-            // drain the row into registers, hand TMEM back, then store
-            uint32_t pk[128];
+            // drain this warp's 128 columns into registers (two loads in flight
+            // at a time), hand TMEM back, then store
+            uint32_t pk[64];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint32_t v[32];
-                tmem_ld32(t_row + c * 32, v);
+            for (int c = 0; c < 4; c += 2) {
+                uint32_t v0[32], v1[32];
+                tmem_ld32(t_row + c * 32, v0);
+                tmem_ld32(t_row + (c + 1) * 32, v1);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    pk[c * 16 + j] = pack2<F16>(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                for (int j = 0; j < 16; ++j) {
+                    pk[c * 16 + j] = pack2<F16>(__uint_as_float(v0[2 * j]), __uint_as_float(v0[2 * j + 1]));
+                    pk[(c + 1) * 16 + j] = pack2<F16>(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1]));
+                }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(acc_empty_r0);
+            if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty_r0);
             if (run && row < pr.m) {
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const int col0 = w.n_tile * 256 + c * 32;
+                for (int c = 0; c < 4; ++c) {
+                    const int col0 = col_base + c * 32;
                     if (col0 < pr.n) {
                         uint32_t part[16];
 #pragma unroll
@@ -457,7 +474,7 @@ cudaError_t launch_pair(const PairParams<MAXG> &params, cudaStream_t stream)
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(2 * pairs, 1, 1);
-    cfg.blockDim = dim3(256, 1, 1);
+    cfg.blockDim = dim3(kPairThreads, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];

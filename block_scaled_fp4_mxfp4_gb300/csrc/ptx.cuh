@@ -90,21 +90,81 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// The same test with the thread's suspension bounded by `hint_ns` (a try_wait
+// otherwise may block for a hardware-chosen time before it reports that the
+// phase is still open).
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    if constexpr (CLUSTER)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+            : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete. Returns false after
-// limit_ns nanoseconds, having recorded `code` in *err (first error wins).
+// limit_ns nanoseconds, having recorded `code` in *err (first error wins). A
+// limit below the default also bounds each try_wait's suspension, so that the
+// limit holds even for waits shorter than the hardware's own suspend time.
 template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err, int code,
                                           uint64_t limit_ns = kWaitTimeoutNs)
 {
-    if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
+    if (limit_ns >= kWaitTimeoutNs) {
+        if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
+        const uint64_t t0 = global_timer_ns();
+        while (true) {
+            if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
+            if (global_timer_ns() - t0 > limit_ns) {
+                atomicCAS(err, 0, code);
+                return false;
+            }
+        }
+    }
+    const uint32_t hint = static_cast<uint32_t>(limit_ns);
     const uint64_t t0 = global_timer_ns();
     while (true) {
-        if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
+        if (mbar_try_wait_hint<CLUSTER>(bar, parity, hint)) return true;
         if (global_timer_ns() - t0 > limit_ns) {
             atomicCAS(err, 0, code);
             return false;
         }
     }
+}
+
+// mbar_wait by every lane of a warp, with one verdict for all: false if any
+// lane gave up (so that the warp leaves a loop together).
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, int *err, int code,
+                                               uint64_t limit_ns = kWaitTimeoutNs)
+{
+    const bool ok = mbar_wait<CLUSTER>(bar, parity, err, code, limit_ns);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// True in exactly one lane of a converged warp (the same lane every time the
+// warp asks with all lanes active).
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(pred)::"memory");
+    return pred != 0;
 }
 
 // Lowers the transaction count of the current phase of `bar` by `bytes`, as
@@ -119,6 +179,13 @@ __device__ __forceinline__ void mbar_complete_tx(uint64_t *bar, uint32_t bytes)
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
 {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Relaxed arrive on an mbarrier of a CTA of this cluster: signals an event
+// without publishing memory (far cheaper than a release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // --------------------------------------------------------------------- TMA
