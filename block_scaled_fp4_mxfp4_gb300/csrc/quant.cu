@@ -9,16 +9,19 @@
 //   codes E2M1_RNE_sat(x / s), s == 0 -> zero magnitudes.
 // Both kernels keep the IEEE sign of every element in code bit 3.
 //
-// Work unit: one warp x up to four consecutive 256-element K segments of one
-// row (fewer when that would leave the grid too small to fill the GPU). For each segment a lane loads one 16-byte vector (8 bf16) -- a warp
-// load covers 512 contiguous bytes -- and stores one 32-bit word of codes (128
-// contiguous bytes per warp); the unit's loads are all issued before any
-// segment is encoded. Scale bytes are gathered with shuffles into 32-bit words
-// (4 consecutive K-blocks of one row, which are contiguous in the blocked
-// layout). Rows past M up to the next multiple of 128 and K-blocks past K
-// inside a written word get the pad byte (0x7F for E8M0 = 1.0, 0x00 for E4M3).
-// One launch may quantize up to kMaxGroups matrices (the grouped path); a
-// single matrix is a table of one.
+// Work unit: one warp x one 1024-element chunk of one row. The warp loads the
+// chunk with 16-byte vectors, 512 contiguous bytes per instruction (the access
+// that streams at full HBM bandwidth), and passes it through a 2 KB shared
+// buffer so that each lane then holds 32 consecutive elements: one MXFP4
+// block or two NVFP4 blocks. A lane takes its blocks' largest magnitudes with
+// packed bf16 max operations, encodes its 16 bytes of codes and stores them
+// with one vector store (the warp writes 512 contiguous bytes); the scale
+// bytes of four consecutive blocks meet in one lane by two (MXFP4) or one
+// (NVFP4) shuffles and go out as one 32-bit word of the blocked layout. Rows
+// past M up to the next multiple of 128 and K-blocks past K inside a written
+// word get the pad byte (0x7F for E8M0 = 1.0, 0x00 for E4M3). One launch may
+// quantize up to kMaxGroups matrices (the grouped path); a single matrix is a
+// table of one.
 #include <cstring>
 
 #include "internal.h"
@@ -29,16 +32,15 @@ namespace mxfp4 {
 namespace {
 
 constexpr int kQuantThreads = 256;
-
-constexpr int kQuantUnroll = 4;     // most segments per work unit, loaded together
-// resident blocks per SM: <= 48 registers a thread for MXFP4, <= 64 for NVFP4
-// (its reciprocal and scale conversions need more)
+constexpr int kQuantWarps = kQuantThreads / 32;
+constexpr int kChunk = 1024;            // elements per work unit (one warp)
+// resident blocks per SM (16 KB of shared memory each): MXFP4 fits in 40
+// registers, NVFP4's reciprocal and scale conversion want a few more
 template <int VEC>
-constexpr int kQuantMinBlocks = VEC == 32 ? 5 : 4;
+constexpr int kQuantBlocksPerSm = VEC == 32 ? 6 : 5;
 
 // The matrices of one launch: the work units of matrix g are the global
-// units [first[g], first[g + 1]), row-major over (padded row, chunk of
-// `chunk` <= kQuantUnroll segments).
+// units [first[g], first[g + 1]), row-major over (row padded to 128, chunk).
 struct QuantGroupsDev {
     const uint16_t *A[kMaxGroups];
     uint8_t *Aq[kMaxGroups];
@@ -46,87 +48,98 @@ struct QuantGroupsDev {
     int64_t lda[kMaxGroups], ldq[kMaxGroups];
     int64_t first[kMaxGroups + 1];
     int M[kMaxGroups], K[kMaxGroups], nchunk[kMaxGroups];
+    int vec_store[kMaxGroups];   // code rows 16-byte aligned: one vector store per lane
     int count;
-    int chunk;
 };
 
-// Encode segment seg of a row (8 elements per lane in v; the row's codes at
-// qrow, its scale words at sfrow + word * 512). VEC = 32 (MXFP4) or 16
-// (NVFP4); lanes per scale block = VEC / 8.
+// Position of 16-byte slot s of a warp's chunk buffer: the slot's bank group
+// (s mod 8) is XORed with (s / 8) mod 8, so that both the loading pattern
+// (slot 32 j + lane) and the reading pattern (slot 4 lane + j) touch eight
+// distinct bank groups in every quarter-warp.
+__device__ __forceinline__ int swz(int s) { return s ^ ((s >> 3) & 7); }
+
 template <int VEC>
-__device__ __forceinline__ void encode_segment(uint4 v, bool row_ok, int seg, int C, int cblocks, uint8_t *qrow,
-                                               uint8_t *sfrow, int lane)
+__global__ void __launch_bounds__(kQuantThreads, kQuantBlocksPerSm<VEC>) quant_kernel(const __grid_constant__ QuantGroupsDev q)
 {
-    constexpr int LPB = VEC / 8;            // lanes per scale block
-    constexpr int BPS = 256 / VEC;          // blocks per 256-element segment (8 or 16)
+    constexpr int BPL = 32 / VEC;                 // blocks per lane (1 or 2)
     constexpr uint32_t PAD = VEC == 32 ? 0x7Fu : 0x00u;
-    const int blk = seg * BPS + lane / LPB;           // scale column of this lane
-    const int k = blk * VEC + (lane % LPB) * 8;       // first element of this lane
-    const bool ok = row_ok && blk < C;
-
-    uint32_t amax = max_abs_bits8(v);
-#pragma unroll
-    for (int o = 1; o < LPB; o <<= 1) amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-
-    uint32_t sbyte;
-    uint32_t codes;
-    if (VEC == 32) {
-        sbyte = e8m0_byte_from_amax(amax);
-        codes = mx_codes8(v, sbyte);
-    } else {
-        sbyte = nv_scale_byte(amax);
-        codes = nv_codes8(v, nv_recip(sbyte));
-    }
-    if (ok) *reinterpret_cast<uint32_t *>(qrow + k / 2) = codes;
-    // scale words: 4 consecutive blocks -> lanes base + j * LPB
-    const uint32_t mine = ok ? sbyte : PAD;
-    constexpr int LANES_PER_WORD = 4 * LPB;      // 16 (MX) or 8 (NV)
-    const int base = lane & ~(LANES_PER_WORD - 1);
-    uint32_t word = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) word |= __shfl_sync(0xffffffffu, mine, base + j * LPB) << (8 * j);
-    const int widx = seg * (BPS / 4) + lane / LANES_PER_WORD;
-    if ((lane & (LANES_PER_WORD - 1)) == 0 && widx < cblocks)
-        *reinterpret_cast<uint32_t *>(sfrow + static_cast<size_t>(widx) * 512) = word;
-}
-
-// Warp w takes the units w, w + W, w + 2W, ... (W warps in the grid).
-template <int VEC>
-__global__ void __launch_bounds__(kQuantThreads, kQuantMinBlocks<VEC>) quant_kernel(const __grid_constant__ QuantGroupsDev q)
-{
-    constexpr int U = kQuantUnroll;
-    constexpr int LPB = VEC / 8;
-    constexpr int BPS = 256 / VEC;
+    __shared__ uint4 chunk_buf[kQuantWarps][kChunk / 8];
+    const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    uint4 *buf = chunk_buf[warp];
     const int64_t units = q.first[q.count];
-    const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kQuantWarps;
     int g = 0;
-    for (int64_t unit = warp0; unit < units; unit += nwarps) {
-        while (unit >= q.first[g + 1]) ++g;     // units only grow along the loop
-        const int64_t local = unit - q.first[g];
-        const int64_t r = local / q.nchunk[g];
-        const int seg0 = static_cast<int>(local - r * q.nchunk[g]) * q.chunk;
+    for (int64_t u = static_cast<int64_t>(blockIdx.x) * kQuantWarps + warp; u < units; u += nwarps) {
+        while (u >= q.first[g + 1]) ++g;         // units only grow along the loop
+        const int64_t local = u - q.first[g];
+        const int nch = q.nchunk[g];
+        const int64_t r = local / nch;
+        const int k0 = static_cast<int>(local - r * nch) * kChunk;
         const int K = q.K[g];
-        const int C = K / VEC;
-        const int cblocks = (C + 3) / 4;
-        const int nseg = (K + 255) / 256;
-        const bool row_ok = r < q.M[g];
-        const uint16_t *arow = q.A[g] + r * q.lda[g];
-        uint4 v[U];
+        const int C = K / VEC;                   // scale columns (K-blocks)
+        const int cblocks = (C + 3) / 4;         // scale words per row
+        const int kl = k0 + 32 * lane;           // first element of this lane's span
+        uint32_t sb[BPL];
 #pragma unroll
-        for (int j = 0; j < U; ++j) {
-            const int blk = (seg0 + j) * BPS + lane / LPB;
-            const int k = blk * VEC + (lane % LPB) * 8;
-            v[j] = make_uint4(0, 0, 0, 0);
-            if (j < q.chunk && row_ok && blk < C) v[j] = ld_nc_v4(arow + k);
+        for (int t = 0; t < BPL; ++t) sb[t] = PAD;
+        if (r < q.M[g]) {
+            const uint16_t *src = q.A[g] + r * q.lda[g] + k0;
+            uint4 v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int e = 256 * j + 8 * lane;
+                v[j] = (k0 + e < K) ? ld_nc_v4(src + e) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) buf[swz(32 * j + lane)] = v[j];
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = buf[swz(4 * lane + j)];
+            __syncwarp();                        // the buffer is free for the next unit
+            if (kl < K) {
+                uint32_t w[4];
+#pragma unroll
+                for (int t = 0; t < BPL; ++t) {
+                    constexpr int NV = VEC / 8;  // 16-byte vectors per block
+                    const uint32_t amax = block_amax_bits<NV>(v + t * NV);
+                    if constexpr (VEC == 32) {
+                        sb[t] = e8m0_byte_from_amax(amax);
+#pragma unroll
+                        for (int i = 0; i < NV; ++i) w[t * NV + i] = mx_codes8(v[t * NV + i], sb[t]);
+                    } else {
+                        sb[t] = nv_scale_byte(amax);
+                        const float rs = nv_recip(sb[t]);
+#pragma unroll
+                        for (int i = 0; i < NV; ++i) w[t * NV + i] = nv_codes8(v[t * NV + i], rs);
+                    }
+                }
+                uint8_t *dst = q.Aq[g] + r * q.ldq[g] + kl / 2;
+                if (q.vec_store[g]) {
+                    *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) reinterpret_cast<uint32_t *>(dst)[i] = w[i];
+                }
+            }
         }
-        uint8_t *qrow = q.Aq[g] + r * q.ldq[g];
-        // the row's first scale word: 128-row chunk, row within a 32-row group, group
-        uint8_t *sfrow = q.sf[g] + (static_cast<size_t>(r >> 7) * cblocks) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
-#pragma unroll
-        for (int j = 0; j < U; ++j)
-            if (j < q.chunk && seg0 + j < nseg) encode_segment<VEC>(v[j], row_ok, seg0 + j, C, cblocks, qrow, sfrow, lane);
+        // four consecutive K-blocks' scale bytes meet in one lane as one word
+        uint32_t word;
+        if constexpr (VEC == 32) {
+            word = sb[0];
+            word |= __shfl_down_sync(0xffffffffu, word, 1) << 8;
+            word |= __shfl_down_sync(0xffffffffu, word, 2) << 16;
+        } else {
+            word = sb[0] | (sb[1] << 8);
+            word |= __shfl_down_sync(0xffffffffu, word, 1) << 16;
+        }
+        constexpr int LPW = 4 / BPL;             // lanes per scale word
+        const int wi = (k0 / VEC + lane * BPL) / 4;
+        if ((lane % LPW) == 0 && wi < cblocks) {
+            // the word's place: 128-row chunk, K-word, row within a 32-row group, group
+            *reinterpret_cast<uint32_t *>(q.sf[g] + ((r >> 7) * cblocks + wi) * 512 + (r & 31) * 16 +
+                                          ((r >> 5) & 3) * 4) = word;
+        }
     }
 }
 
@@ -137,6 +150,7 @@ cudaError_t launch_quant(const QuantGroupHost *groups, int count, int num_sms, c
     QuantGroupsDev q;
     memset(&q, 0, sizeof(q));
     q.count = count;
+    q.first[0] = 0;
     for (int g = 0; g < count; ++g) {
         const QuantGroupHost &h = groups[g];
         if (h.M < 1 || h.K < 1 || h.M > 0x7fffffff || h.K > 0x7fffffff) return cudaErrorInvalidValue;
@@ -147,24 +161,14 @@ cudaError_t launch_quant(const QuantGroupHost *groups, int count, int num_sms, c
         q.K[g] = static_cast<int>(h.K);
         q.lda[g] = h.lda;
         q.ldq[g] = h.ldq;
-    }
-    // the longest chunk that still gives every SM a resident wave of warps
-    // (small matrices fall back to one segment per unit, all loads in flight)
-    const int64_t want_units = static_cast<int64_t>(num_sms) * kQuantMinBlocks<VEC> * (kQuantThreads / 32);
-    for (int chunk = kQuantUnroll; chunk >= 1; chunk /= 2) {
-        q.chunk = chunk;
-        q.first[0] = 0;
-        for (int g = 0; g < count; ++g) {
-            q.nchunk[g] = static_cast<int>(((q.K[g] + 255) / 256 + chunk - 1) / chunk);
-            q.first[g + 1] = q.first[g] + (static_cast<int64_t>(q.M[g]) + 127) / 128 * 128 * q.nchunk[g];
-        }
-        if (q.first[count] >= want_units) break;
+        q.nchunk[g] = static_cast<int>((h.K + kChunk - 1) / kChunk);
+        q.vec_store[g] = ((reinterpret_cast<uintptr_t>(h.Aq) & 15u) == 0 && (h.ldq & 15) == 0) ? 1 : 0;
+        q.first[g + 1] = q.first[g] + (h.M + 127) / 128 * 128 * q.nchunk[g];
     }
     for (int g = count + 1; g <= kMaxGroups; ++g) q.first[g] = q.first[count];
     const int64_t units = q.first[count];
-    const int64_t per_block = kQuantThreads / 32;
-    int64_t blocks = (units + per_block - 1) / per_block;
-    const int64_t cap = static_cast<int64_t>(num_sms) * kQuantMinBlocks<VEC>;
+    int64_t blocks = (units + kQuantWarps - 1) / kQuantWarps;
+    const int64_t cap = static_cast<int64_t>(num_sms) * kQuantBlocksPerSm<VEC>;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     quant_kernel<VEC><<<static_cast<unsigned>(blocks), kQuantThreads, 0, stream>>>(q);

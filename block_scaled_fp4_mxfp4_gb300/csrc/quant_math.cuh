@@ -55,6 +55,26 @@ __device__ __forceinline__ uint32_t max_abs_bits8(const uint4 &v)
     return max(m & 0xFFFFu, m >> 16);
 }
 
+// Lane-wise bf16 maximum of |a| and |b| (the sign bit of each result lane is
+// not meaningful: mask it off). Finite inputs only.
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// bf16 bits of the largest magnitude among the 8 * N values of v[0 .. N).
+template <int N>
+__device__ __forceinline__ uint32_t block_amax_bits(const uint4 *v)
+{
+    uint32_t m = absmax_bf16x2(absmax_bf16x2(v[0].x, v[0].y), absmax_bf16x2(v[0].z, v[0].w));
+#pragma unroll
+    for (int i = 1; i < N; ++i)
+        m = absmax_bf16x2(m, absmax_bf16x2(absmax_bf16x2(v[i].x, v[i].y), absmax_bf16x2(v[i].z, v[i].w)));
+    return max(m & 0x7FFFu, (m >> 16) & 0x7FFFu);
+}
+
 // E8M0 byte of a block whose largest magnitude has bf16 bits `amax_bits`:
 // floor(log2 amax) = E - 127 for a normal bf16 with exponent field E, so the
 // byte is E - 2; zero, subnormal and E = 1 all clamp to byte 0 (2^-127).
