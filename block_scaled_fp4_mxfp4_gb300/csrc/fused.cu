@@ -10,23 +10,27 @@
 //   accumulator is D[n][m] = C^T, 128 TMEM lanes x MMA_N columns.
 // * Grid = (ceil(N/128) weight tiles) x (S K-splits); the S CTAs of one weight
 //   tile form a thread-block cluster. Each CTA streams its K-slice of 128
-//   weight rows through a 4-slot TMA ring (evict-first: weights are read once).
-// * Warps 2-5 are stage warps: warp 2 + w owns the CTA's K-stages w, w + 4, ...
-//   Its lanes read the stage's bf16 A straight from global memory (a batch of
-//   loads in flight per lane), form the OCP MX scale and the E2M1 codes of each
-//   32-element block with the same arithmetic as the standalone quant kernel,
-//   and write them into shared memory directly in the MMA's 128-byte-swizzled
-//   K-major operand layout, plus the scales in the 512-byte blocked layout.
-//   Lane 0 then copies both operands' scales to TMEM and issues the stage's
-//   MMAs into the warp's own TMEM accumulator. Issuing a tcgen05 instruction
-//   costs on the order of 100 cycles while an N = 16 MMA is only a few cycles
-//   of tensor work, so the four stage warps issue in parallel and the
-//   epilogue sums their accumulators.
-// * Split-K reduction without global scratch: every CTA pushes the slice of
-//   its fp32 tile that CTA r of the cluster owns (weight rows r*128/S ..) into
-//   r's shared memory with remote stores; after one cluster barrier each CTA
-//   sums its slice over the S sources in rank order and writes bf16 C. The
-//   sum order is fixed, so results are deterministic.
+//   weight rows through a 4-slot TMA ring (evict-first: weights are read once);
+//   the first four stages are requested before the grid-dependency wait.
+// * Eight warps in four groups of 64 threads: group s owns ring slot s and
+//   the CTA's K-stages s, s + 4, ... For each of its stages the group's
+//   threads read the stage's bf16 A straight from global memory, two 32-element
+//   blocks per thread at MMA_N = 16 (so that quantizing a stage takes one short
+//   pass rather than a long serial loop in one warp), form the OCP MX scale and
+//   E2M1 codes with the same arithmetic as the standalone quant kernel, and
+//   write them into shared memory in the MMA's 128-byte-swizzled K-major
+//   operand layout, the scales in the 512-byte blocked layout. After a named
+//   barrier of the group its first thread copies both operands' scales to
+//   TMEM and issues the stage's MMAs into the group's own TMEM accumulator
+//   (issuing a tcgen05 instruction costs on the order of 100 cycles while an
+//   N = 16 MMA is only a few cycles of tensor work, so the four groups issue in
+//   parallel), then refills its ring slot with its next stage's weights.
+// * Split-K reduction without global scratch: every CTA sums the four group
+//   accumulators and pushes the slice of the fp32 tile that CTA r of the
+//   cluster owns (weight rows r*128/S ..) into r's shared memory with remote
+//   stores; after one cluster barrier each CTA sums its slice over the S
+//   sources in rank order and writes C. The sum order is fixed, so results are
+//   deterministic.
 // Shared memory stays near 100 KB (MMA_N = 16) so two CTAs fit on an SM and
 // every cluster of the grid can be resident at once.
 #include <cstring>
@@ -47,10 +51,14 @@ constexpr uint32_t kWBytes = 128 * 128;   // one stage of 128 weight rows x 256 
 // MXFP4 (E8M0 per 32, kind::mxf4, bf16 C).
 template <bool NV>
 constexpr int kSfBlk = NV ? 4 : 2;         // 512-byte scale blocks per 128 rows per stage
-constexpr int kThreads = 192;
-constexpr int kStageWarps = 4;           // warps 2-5: quantize + issue MMAs
+// 256 threads: measured on the 16 x 2112 x 7168 call against 128 and 512
+// (6.07 and 6.33 us per call against 5.78)
+constexpr int kThreads = 256;
+constexpr int kGroups = 4;                // warp groups; group s owns ring slot s
+constexpr int kGroupThreads = kThreads / kGroups;
+constexpr int kEpiParts = kThreads / 128;  // warps per TMEM lane quadrant in the epilogue
 constexpr int kMaxSplits = 8;             // portable cluster size
-constexpr int kBatch = 4;                 // 32-element blocks a lane keeps in flight
+static_assert(kGroups == kRing, "a group refills its own ring slot");
 
 __host__ __device__ constexpr uint32_t pow2_cols_f(uint32_t n)
 {
@@ -65,7 +73,7 @@ struct FusedCfg {
     // and its own TMEM scale columns (fewer with NVFP4's larger scale blocks,
     // so that two CTAs still share an SM).
     static constexpr int MAX_ST = MMA_N <= 16 ? (NV ? 6 : 8) : 4;
-    static constexpr int BPL = MMA_N * 8 / 32;              // 32-blocks per lane per stage
+    static constexpr int UPT = MMA_N * 8 / kGroupThreads;   // 32-element blocks per thread per stage
     static constexpr uint32_t ACT_TILE = MMA_N * 128;       // quantized operand bytes per stage
     static constexpr uint32_t RING_DATA = kRing * kWBytes;
     static constexpr uint32_t ACT_OFF = RING_DATA;
@@ -77,9 +85,9 @@ struct FusedCfg {
     static constexpr uint32_t BAR_OFF = RECV_OFF + RECV_BYTES;
     static constexpr uint32_t SMEM_BYTES = BAR_OFF + 256 + 1024;
     static constexpr uint32_t SF_COLS = 2 * SF_BLK * 4;      // per stage: weight + activation blocks
-    static constexpr uint32_t ACC_COLS = kStageWarps * MMA_N;  // one accumulator per stage warp
+    static constexpr uint32_t ACC_COLS = kGroups * MMA_N;   // one accumulator per warp group
     static constexpr uint32_t TMEM_COLS = pow2_cols_f(ACC_COLS + MAX_ST * SF_COLS);
-    static_assert(BPL % kBatch == 0, "quant work split");
+    static_assert(UPT >= 1 && UPT * kGroupThreads == MMA_N * 8, "quant work split");
     static_assert(ACT_TILE % 1024 == 0, "swizzled operand tiles need 1024-byte alignment");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(ACC_COLS + MAX_ST * SF_COLS <= 512, "TMEM budget");
@@ -109,6 +117,35 @@ __device__ __forceinline__ uint16_t to_c(float f)
         return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
+__device__ __forceinline__ void group_bar(int grp)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "n"(kGroupThreads) : "memory");
+}
+
+// Sum of the `nacc` group accumulators' columns [c0, c0 + W) of this warp's
+// TMEM lane quadrant (row base t_row).
+template <int W>
+__device__ __forceinline__ void sum_accumulators(uint32_t t_row, int c0, int nacc, int stride, float (&f)[W])
+{
+#pragma unroll
+    for (int j = 0; j < W; ++j) f[j] = 0.0f;
+    for (int a = 0; a < nacc; ++a) {
+        uint32_t v[W];
+        const uint32_t addr = t_row + static_cast<uint32_t>(a * stride + c0);
+        if constexpr (W == 4)
+            tmem_ld4(addr, v);
+        else if constexpr (W == 8)
+            tmem_ld8(addr, v);
+        else if constexpr (W == 16)
+            tmem_ld16(addr, v);
+        else
+            tmem_ld32(addr, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < W; ++j) f[j] += __uint_as_float(v[j]);
+    }
+}
+
 template <int MMA_N, bool NV>
 __global__ void __launch_bounds__(kThreads, 2)
     fused_quant_gemm_kernel(const __grid_constant__ CUtensorMap tmw, const FusedArgs p)
@@ -123,13 +160,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     float *recv = reinterpret_cast<float *>(smem + Cfg::RECV_OFF);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::BAR_OFF);
     uint64_t *empty = full + kRing;
-    uint64_t *accf = empty + kRing;              // one arrival per stage warp
+    uint64_t *accf = empty + kRing;              // one arrival per warp group
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accf + 1);
     volatile int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
     volatile int *abort_in = abort_flag + 1;    // [kMaxSplits] the abort flag of each CTA of the cluster
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int grp = warp / (kGroupThreads / 32);
+    const int gt = threadIdx.x % kGroupThreads;  // thread index within the group
+    const bool leader = gt == 0;                 // issues the group's copies and tcgen05 instructions
     const int n_tile = blockIdx.x;
     const int split = blockIdx.y;
     const int k_stages = (p.K + 255) / 256;
@@ -138,7 +178,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int nst = s_end - s_begin;
     const int k_steps_total = (p.K + 63) / 64;
 
-    int issued = 0;
     const uint64_t pol_w = policy_evict_first();   // weights are read once
     auto issue_weights = [&](int i) {
         const int slot = i % kRing;
@@ -149,15 +188,22 @@ __global__ void __launch_bounds__(kThreads, 2)
         tma_load_2d(ring + slot * kWBytes, &tmw, ks * 128, n_tile * 128, full + slot, pol_w);
         bulk_load(ring_sf + slot * Cfg::SF_STAGE, p.sfw + (static_cast<size_t>(n_tile) * p.sf_cblocks + blk0) * 512,
                   nblk * 512, full + slot, pol_w);
-        issued = i + 1;
     };
+    if (threadIdx.x == 0 && nst > 0) {
+        // Warm L2 with this CTA's rows of A before the weight stream is
+        // requested; the loads that use A still wait for that grid below.
+        const int64_t k0 = static_cast<int64_t>(s_begin) * 256;
+        const int64_t k1 = min(static_cast<int64_t>(s_end) * 256, static_cast<int64_t>(p.K));
+        for (int m = 0; m < p.M; ++m)
+            prefetch_l2_bulk(p.A + static_cast<int64_t>(m) * p.lda + k0, static_cast<uint32_t>((k1 - k0) * 2));
+    }
     if (threadIdx.x == 0) {
 #pragma unroll
         for (int s = 0; s < kRing; ++s) {
             mbar_init(full + s, 1);
             mbar_init(empty + s, 1);
         }
-        mbar_init(accf, kStageWarps);
+        mbar_init(accf, kGroups);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmw);
@@ -171,13 +217,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
         tmem_relinquish();
     }
-    if (threadIdx.x >= 64 && threadIdx.x - 64 < p.M && nst > 0) {
-        // Warm L2 with this CTA's rows of A while the preceding grid finishes;
-        // the loads that use A still wait for that grid below.
-        const int64_t k0 = static_cast<int64_t>(s_begin) * 256;
-        const int64_t k1 = min(static_cast<int64_t>(s_end) * 256, static_cast<int64_t>(p.K));
-        prefetch_l2_bulk(p.A + static_cast<int64_t>(threadIdx.x - 64) * p.lda + k0, static_cast<uint32_t>((k1 - k0) * 2));
-    }
+
     // A, C and everything else in global memory is touched only after the
     // preceding grid in the stream has completed and its writes are visible.
     grid_dependency_wait();
@@ -186,141 +226,134 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        if (lane == 0) {
-            // ------------------------------- weight TMA producer (stages past the ring)
-            for (int i = kRing; i < nst; ++i) {
-                const int slot = i % kRing;
-                if (!mbar_wait(empty + slot, ((i / kRing) - 1) & 1, &g_fused_error, kErrWaitEmpty, p.wait_ns)) {
-                    *abort_flag = 1;
-                    break;
-                }
-                issue_weights(i);
+    // --------------------- warp groups: quantize a K-stage of A, issue its MMAs
+    // Group grp owns stages t = grp, grp + 4, ... and ring slot grp. Its
+    // threads quantize the stage's MMA_N x 8 blocks of 32 elements (thread gt
+    // takes blocks gt + 128 x), writing codes in the MMA's 128-byte-swizzled
+    // K-major layout and scales in the blocked layout. Rows >= M and blocks
+    // past K are zero and quantize to code 0 with scale byte 0.
+    const int slot = grp;
+    const uint32_t acc_tmem = tmem + static_cast<uint32_t>(grp * MMA_N);
+    constexpr uint32_t IDESC = idesc_block_scaled(MMA_N, !NV);
+    int last_issued = grp < min(nst, kRing) ? grp : -1;   // latest stage requested into this slot
+    bool first = true;
+    for (int t = grp; t < nst; t += kGroups) {
+        const int ks = s_begin + t;
+        if (t >= kRing && leader) {
+            // the slot's previous stage has been consumed once its MMAs are done
+            if (!mbar_wait(empty + slot, ((t / kRing) - 1) & 1, &g_fused_error, kErrWaitEmpty, p.wait_ns)) {
+                *abort_flag = 1;
+            } else {
+                issue_weights(t);
+                last_issued = t;
             }
         }
-    } else if (warp >= 2) {
-        // --------------- stage warps: quantize a K-stage of A, then issue its MMAs
-        // Stage warp sw owns stages t = sw, sw + 4, ...: its lanes quantize the
-        // stage's MMA_N x 8 blocks of 32 elements (lane owns blocks lane + 32 e),
-        // writing codes in the MMA's 128-byte-swizzled K-major layout and scales
-        // in the blocked layout; lane 0 then copies both operands' scales to
-        // TMEM and issues the stage's four MMAs into the warp's own accumulator,
-        // so the stages of a CTA are quantized and issued in parallel. Rows >= M
-        // and blocks past K are zero and quantize to code 0 with scale byte 0.
-        const int sw = warp - 2;
-        const uint32_t acc_tmem = tmem + static_cast<uint32_t>(sw * MMA_N);
-        constexpr uint32_t IDESC = idesc_block_scaled(MMA_N, !NV);
-        bool first = true;
-        for (int t = sw; t < nst; t += kStageWarps) {
-            const int ks = s_begin + t;
-            uint8_t *dst = act + t * Cfg::ACT_TILE;
-            uint8_t *dsf = act_sf + t * Cfg::SF_STAGE;
+        uint8_t *dst = act + t * Cfg::ACT_TILE;
+        uint8_t *dsf = act_sf + t * Cfg::SF_STAGE;
+        constexpr int BATCH = Cfg::UPT < 2 ? Cfg::UPT : 2;   // blocks whose loads are in flight together
 #pragma unroll 1
-            for (int e0 = 0; e0 < Cfg::BPL; e0 += kBatch) {
-                uint4 v[kBatch][4];
+        for (int x0 = 0; x0 < Cfg::UPT; x0 += BATCH) {
+            uint4 v[BATCH][4];
 #pragma unroll
-                for (int x = 0; x < kBatch; ++x) {
-                    const int u = lane + 32 * (e0 + x);
-                    const int m = u >> 3, j = u & 7;
-                    const int k0 = ks * 256 + j * 32;
-                    const bool ok = m < p.M && k0 < p.K;
-                    const uint16_t *src = p.A + static_cast<int64_t>(m) * p.lda + k0;
+            for (int x = 0; x < BATCH; ++x) {
+                const int u = gt + kGroupThreads * (x0 + x);
+                const int m = u >> 3, j = u & 7;
+                const int k0 = ks * 256 + j * 32;
+                const bool ok = m < p.M && k0 < p.K;
+                const uint16_t *src = p.A + static_cast<int64_t>(m) * p.lda + k0;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) v[x][q] = ok ? ld_nc_v4(src + q * 8) : make_uint4(0, 0, 0, 0);
-                }
+                for (int q = 0; q < 4; ++q) v[x][q] = ok ? ld_nc_v4(src + q * 8) : make_uint4(0, 0, 0, 0);
+            }
 #pragma unroll
-                for (int x = 0; x < kBatch; ++x) {
-                    const int u = lane + 32 * (e0 + x);
-                    const int m = u >> 3, j = u & 7;
-                    uint4 codes;
-                    if constexpr (NV) {
-                        // two 16-element groups, each with s = E4M3(fp32(amax) / 6)
-                        // and codes of x / s, as the standalone NVFP4 quantizer
+            for (int x = 0; x < BATCH; ++x) {
+                const int u = gt + kGroupThreads * (x0 + x);
+                const int m = u >> 3, j = u & 7;
+                uint4 codes;
+                if constexpr (NV) {
+                    // two 16-element groups, each with s = E4M3(fp32(amax) / 6)
+                    // and codes of x / s, as the standalone NVFP4 quantizer
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const uint32_t pr = umax16x2(max_abs_pair8(v[x][2 * h]), max_abs_pair8(v[x][2 * h + 1]));
-                            const uint32_t amax = max(pr & 0xFFFFu, pr >> 16);
-                            const uint32_t sbyte = nv_scale_byte(amax);
-                            const float rs = nv_recip(sbyte);
-                            const uint32_t lo = nv_codes8(v[x][2 * h], rs), hi = nv_codes8(v[x][2 * h + 1], rs);
-                            if (h == 0) {
-                                codes.x = lo;
-                                codes.y = hi;
-                            } else {
-                                codes.z = lo;
-                                codes.w = hi;
-                            }
-                            const int c = 2 * j + h;   // scale column within the stage (16 per stage)
-                            dsf[(c >> 2) * 512 + (m & 31) * 16 + (m >> 5) * 4 + (c & 3)] = static_cast<uint8_t>(sbyte);
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t sbyte = nv_scale_byte(block_amax_bits<2>(&v[x][2 * h]));
+                        const float rs = nv_recip(sbyte);
+                        const uint32_t lo = nv_codes8(v[x][2 * h], rs), hi = nv_codes8(v[x][2 * h + 1], rs);
+                        if (h == 0) {
+                            codes.x = lo;
+                            codes.y = hi;
+                        } else {
+                            codes.z = lo;
+                            codes.w = hi;
                         }
-                    } else {
-                        const uint32_t pair = umax16x2(umax16x2(max_abs_pair8(v[x][0]), max_abs_pair8(v[x][1])),
-                                                       umax16x2(max_abs_pair8(v[x][2]), max_abs_pair8(v[x][3])));
-                        const uint32_t sbyte = e8m0_byte_from_amax(max(pair & 0xFFFFu, pair >> 16));
-                        codes.x = mx_codes8(v[x][0], sbyte);
-                        codes.y = mx_codes8(v[x][1], sbyte);
-                        codes.z = mx_codes8(v[x][2], sbyte);
-                        codes.w = mx_codes8(v[x][3], sbyte);
-                        dsf[(j >> 2) * 512 + (m & 31) * 16 + (m >> 5) * 4 + (j & 3)] = static_cast<uint8_t>(sbyte);
+                        const int c = 2 * j + h;   // scale column within the stage (16 per stage)
+                        dsf[(c >> 2) * 512 + (m & 31) * 16 + (m >> 5) * 4 + (c & 3)] = static_cast<uint8_t>(sbyte);
                     }
-                    *reinterpret_cast<uint4 *>(dst + m * 128 + ((j ^ (m & 7)) << 4)) = codes;
-                }
-            }
-            fence_proxy_async_smem();   // generic-proxy writes -> visible to tcgen05
-            __syncwarp();
-            if (lane == 0) {
-                const int slot = t % kRing;
-                if (!mbar_wait(full + slot, (t / kRing) & 1, &g_fused_error, kErrWaitFull, p.wait_ns)) {
-                    *abort_flag = 1;
                 } else {
-                    tc_fence_after();
-                    const uint32_t w_base = smem_u32(ring + slot * kWBytes);
-                    const uint32_t a_base = smem_u32(dst);
-                    const uint32_t wsf = smem_u32(ring_sf + slot * Cfg::SF_STAGE);
-                    const uint32_t asf = smem_u32(dsf);
-                    const uint32_t tsfw = tmem + Cfg::ACC_COLS + t * Cfg::SF_COLS;
-                    const uint32_t tsfa = tsfw + Cfg::SF_BLK * 4;
-                    const int ksteps = min(4, k_steps_total - ks * 4);
-                    const int nblk = NV ? ksteps : (ksteps + 1) / 2;
-                    for (int b = 0; b < nblk; ++b) {
-                        tc_cp_scale_block(tsfw + b * 4, sdesc_scale(wsf + b * 512));
-                        tc_cp_scale_block(tsfa + b * 4, sdesc_scale(asf + b * 512));
-                    }
-                    for (int kk = 0; kk < ksteps; ++kk) {
-                        const uint32_t sfid = NV ? 0u : static_cast<uint32_t>(kk & 1) * 2u;
-                        const int blk = NV ? kk : kk >> 1;
-                        const uint32_t idesc = idesc_with_sf_ids(IDESC, sfid, sfid);
-                        const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-                        if constexpr (NV)
-                            mma_nvf4(acc_tmem, sdesc_sw128(w_base + kk * 32), sdesc_sw128(a_base + kk * 32), idesc,
-                                     tsfw + blk * 4, tsfa + blk * 4, acc);
-                        else
-                            mma_mxf4(acc_tmem, sdesc_sw128(w_base + kk * 32), sdesc_sw128(a_base + kk * 32), idesc,
-                                     tsfw + blk * 4, tsfa + blk * 4, acc);
-                    }
-                    tc_commit(empty + slot);
+                    const uint32_t sbyte = e8m0_byte_from_amax(block_amax_bits<4>(v[x]));
+                    codes.x = mx_codes8(v[x][0], sbyte);
+                    codes.y = mx_codes8(v[x][1], sbyte);
+                    codes.z = mx_codes8(v[x][2], sbyte);
+                    codes.w = mx_codes8(v[x][3], sbyte);
+                    dsf[(j >> 2) * 512 + (m & 31) * 16 + (m >> 5) * 4 + (j & 3)] = static_cast<uint8_t>(sbyte);
                 }
+                *reinterpret_cast<uint4 *>(dst + m * 128 + ((j ^ (m & 7)) << 4)) = codes;
             }
-            first = false;
-            __syncwarp();
         }
-        // one arrival per stage warp once its MMAs are done (at once if it had none)
-        if (lane == 0) {
-            if (first)
-                mbar_arrive(accf);
-            else
-                tc_commit(accf);
+        fence_proxy_async_smem();   // generic-proxy writes -> visible to tcgen05
+        group_bar(grp);             // the stage's operand and scales are complete
+        if (leader) {
+            if (!mbar_wait(full + slot, (t / kRing) & 1, &g_fused_error, kErrWaitFull, p.wait_ns)) {
+                *abort_flag = 1;
+            } else {
+                tc_fence_after();
+                const uint32_t w_base = smem_u32(ring + slot * kWBytes);
+                const uint32_t a_base = smem_u32(dst);
+                const uint32_t wsf = smem_u32(ring_sf + slot * Cfg::SF_STAGE);
+                const uint32_t asf = smem_u32(dsf);
+                const uint32_t tsfw = tmem + Cfg::ACC_COLS + t * Cfg::SF_COLS;
+                const uint32_t tsfa = tsfw + Cfg::SF_BLK * 4;
+                const int ksteps = min(4, k_steps_total - ks * 4);
+                const int nblk = NV ? ksteps : (ksteps + 1) / 2;
+                for (int b = 0; b < nblk; ++b) {
+                    tc_cp_scale_block(tsfw + b * 4, sdesc_scale(wsf + b * 512));
+                    tc_cp_scale_block(tsfa + b * 4, sdesc_scale(asf + b * 512));
+                }
+                for (int kk = 0; kk < ksteps; ++kk) {
+                    const uint32_t sfid = NV ? 0u : static_cast<uint32_t>(kk & 1) * 2u;
+                    const int blk = NV ? kk : kk >> 1;
+                    const uint32_t idesc = idesc_with_sf_ids(IDESC, sfid, sfid);
+                    const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+                    if constexpr (NV)
+                        mma_nvf4(acc_tmem, sdesc_sw128(w_base + kk * 32), sdesc_sw128(a_base + kk * 32), idesc,
+                                 tsfw + blk * 4, tsfa + blk * 4, acc);
+                    else
+                        mma_mxf4(acc_tmem, sdesc_sw128(w_base + kk * 32), sdesc_sw128(a_base + kk * 32), idesc,
+                                 tsfw + blk * 4, tsfa + blk * 4, acc);
+                }
+                tc_commit(empty + slot);
+            }
         }
+        first = false;
     }
-    __syncwarp();
+    // one arrival per group once its MMAs are done (at once if it had none)
+    if (leader) {
+        if (first)
+            mbar_arrive(accf);
+        else
+            tc_commit(accf);
+    }
 
     // -------------------------------------------------------------- epilogue
+    // Warp w reads TMEM lane quadrant w % 4 and columns [CPW (w / 4), + CPW)
+    // of every group accumulator, sums them and pushes (or stores) its part.
     const int S = p.splits;
     const int nper = (128 + S - 1) / S;           // weight rows each CTA of the cluster owns
-    const int nacc = min(nst, kStageWarps);       // accumulators that hold data
-    if (warp >= 2) {
-        // a stage warp that gave up set the abort flag before its arrival on accf
-        const bool acc_ok = mbar_wait(accf, 0, &g_fused_error, kErrWaitAccum, p.wait_ns) && *abort_flag == 0;
+    const int nacc = min(nst, kGroups);           // accumulators that hold data
+    constexpr int CPW = MMA_N / kEpiParts;        // accumulator columns per warp
+    {
+        // a group that gave up set the abort flag before its arrival on accf
+        int acc_ok = 1;
+        if (lane == 0) acc_ok = mbar_wait(accf, 0, &g_fused_error, kErrWaitAccum, p.wait_ns) && *abort_flag == 0;
+        acc_ok = __shfl_sync(0xffffffffu, acc_ok, 0);
         // The next grid in the stream may start once the accumulators are
         // complete. Its weight stream then overlaps this grid's reduction and
         // exit instead of competing with this grid's loads of A (measured on
@@ -329,40 +362,31 @@ __global__ void __launch_bounds__(kThreads, 2)
         grid_launch_dependents();
         tc_fence_after();
         const int q = warp & 3;                      // TMEM lane quadrant of this warp
+        const int c0 = (warp >> 2) * CPW;
         const int n_local = q * 32 + lane;
         const int n = n_tile * 128 + n_local;
         const uint32_t t_row = tmem + (static_cast<uint32_t>(q * 32) << 16);
-        const int owner = n_local / nper;
-        const uint32_t dst_base =
-            S > 1 ? mapa_shared(smem_u32(recv) + static_cast<uint32_t>(split * MMA_N * nper + (n_local - owner * nper)) * 4,
-                                static_cast<uint32_t>(owner))
-                  : 0u;
-#pragma unroll 1
-        for (int c0 = 0; c0 < MMA_N; c0 += 16) {
-            float f[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) f[j] = 0.0f;
-            for (int a = 0; a < nacc; ++a) {
-                uint32_t v[16];
-                tmem_ld16(t_row + static_cast<uint32_t>(a * MMA_N + c0), v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 16; ++j) f[j] += __uint_as_float(v[j]);
-            }
-            if (!acc_ok) continue;
+        float f[CPW];
+        sum_accumulators<CPW>(t_row, c0, nacc, MMA_N, f);
+        if (acc_ok) {
             if (S == 1) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
+                for (int j = 0; j < CPW; ++j) {
                     const int m = c0 + j;
                     if (m < p.M && n < p.N) p.C[static_cast<int64_t>(m) * p.ldc + n] = to_c<NV>(f[j]);
                 }
             } else {
+                const int owner = n_local / nper;
+                const uint32_t dst_base = mapa_shared(
+                    smem_u32(recv) + static_cast<uint32_t>(split * MMA_N * nper + (n_local - owner * nper)) * 4,
+                    static_cast<uint32_t>(owner));
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
+                for (int j = 0; j < CPW; ++j)
                     if (c0 + j < p.M) st_shared_cluster_f32(dst_base + (c0 + j) * nper * 4, f[j]);
             }
+        } else {
+            *abort_flag = 1;
         }
-        if (!acc_ok) *abort_flag = 1;
     }
 
     if (S > 1) {
@@ -396,14 +420,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     // -------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
-    if (warp == 0 && lane == 0) {
-        // copies still in flight (only after an abort) must land before exit
-        for (int i = max(0, issued - kRing); i < issued; ++i)
-            mbar_wait(full + (i % kRing), (i / kRing) & 1, &g_fused_error, kErrWaitDrain);
+    if (leader && last_issued >= 0) {
+        // this slot's last copy (still in flight only after an abort) must land
+        // before exit
+        mbar_wait(full + slot, (last_issued / kRing) & 1, &g_fused_error, kErrWaitDrain);
     }
     if (warp == 1) {
-        // every stage warp arrives on accf once all of its MMAs and scale copies
-        // have completed (at once when the epilogue already saw it)
+        // every group arrives on accf once all of its MMAs and scale copies have
+        // completed (at once when the epilogue already saw it)
         if (lane == 0) mbar_wait(accf, 0, &g_fused_error, kErrWaitDrain);
         __syncwarp();
         tc_fence_after();
