@@ -84,7 +84,7 @@ bool encoder()
 struct MapKey {
     uintptr_t ptr;
     int64_t inner, rows, stride;
-    int box_rows, dev, kind;   // kind 0: packed FP4 (u8, 128B swizzle); 1: scale blocks (u32)
+    int box_rows, dev, kind;   // kind 0: packed FP4 (u8, 128B swizzle); 1: scale blocks (u32); 2: C (16-bit)
     bool operator==(const MapKey &o) const
     {
         return ptr == o.ptr && inner == o.inner && rows == o.rows && stride == o.stride &&
@@ -110,7 +110,8 @@ std::mutex g_map_mu;
 std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
 
 mxfp4_status_t cached_map(const MapKey &key, const void *base, CUtensorMapDataType dtype, cuuint64_t inner,
-                          cuuint32_t box_inner, CUtensorMapSwizzle swz, CUtensorMap *out)
+                          cuuint32_t box_inner, CUtensorMapSwizzle swz, CUtensorMap *out,
+                          CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B)
 {
     {
         std::lock_guard<std::mutex> lk(g_map_mu);
@@ -127,8 +128,7 @@ mxfp4_status_t cached_map(const MapKey &key, const void *base, CUtensorMapDataTy
     cuuint32_t box[2] = {box_inner, static_cast<cuuint32_t>(key.box_rows)};
     cuuint32_t estr[2] = {1u, 1u};
     CUresult r = g_encode(&tm, dtype, 2, const_cast<void *>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return MXFP4_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_map_mu);
     if (g_maps.size() > 4096) g_maps.clear();
@@ -158,6 +158,23 @@ mxfp4_status_t sf_map(const void *base, int64_t blocks, int box_blocks, CUtensor
     cudaGetDevice(&dev);
     MapKey key{reinterpret_cast<uintptr_t>(base), 128, blocks, 512, box_blocks, dev, 1};
     return cached_map(key, base, CU_TENSOR_MAP_DATA_TYPE_UINT32, 128u, 128u, CU_TENSOR_MAP_SWIZZLE_NONE, out);
+}
+
+// Tensor map of a 16-bit C [rows, cols] (row stride ld elements) for the
+// single-CTA GEMM's TMA-store epilogue: box {32, 32}, 64-byte swizzle. Sets
+// *usable = false (and succeeds) when C's base or row stride is not 16-byte
+// aligned; the kernel then stores C directly.
+mxfp4_status_t c_map(void *C, int64_t cols, int64_t rows, int64_t ld, CUtensorMap *out, bool *usable)
+{
+    *usable = false;
+    if ((reinterpret_cast<uintptr_t>(C) & 15u) != 0 || (ld * 2) % 16 != 0) return MXFP4_OK;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    MapKey key{reinterpret_cast<uintptr_t>(C), cols, rows, ld * 2, 32, dev, 2};
+    const mxfp4_status_t st = cached_map(key, C, CU_TENSOR_MAP_DATA_TYPE_UINT16, static_cast<cuuint64_t>(cols), 32u,
+                                         CU_TENSOR_MAP_SWIZZLE_64B, out, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    if (st == MXFP4_OK) *usable = true;
+    return st;
 }
 
 // ------------------------------------------------------------- validation
@@ -307,6 +324,10 @@ mxfp4_status_t run_gemm(const void *Aq, int64_t ldaq, const void *A_sf, const vo
         if (st != MXFP4_OK) return st;
         return cuda_status(launch_gemm_mx_pair(h, stream));
     }
+    if (gp.splits == 1 && !epi.on) {
+        st = c_map(C, N, M, ldc, &h.tmc, &h.c_tma);
+        if (st != MXFP4_OK) return st;
+    }
     return cuda_status(launch_gemm_mx(h, gp.bn, gp.splits, part, tickets, stream));
 }
 
@@ -366,6 +387,10 @@ mxfp4_status_t group_gemm(const Problem *problems, int num_groups, bool nv, void
             if (st != MXFP4_OK) return st;
             st = sf_map(p.sfb, static_cast<int64_t>(sf_bytes(p.n, p.k, vec) / 512), pair_sf_box_blocks(nv),
                         &hp[g].tmsfb);
+            if (st != MXFP4_OK) return st;
+        }
+        if (!pair) {
+            st = c_map(p.c, p.n, p.m, p.ldc, &hp[g].tmc, &hp[g].c_tma);
             if (st != MXFP4_OK) return st;
         }
         hp[g].sfa = static_cast<const uint8_t *>(p.sfa);

@@ -87,7 +87,8 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
     constexpr bool MX = Cfg::MX;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * Cfg::STAGE_BYTES);
+    uint8_t *epi_buf = smem + STAGES * Cfg::STAGE_BYTES;   // [epilogue warp][2][2 KB] when Cfg::TMA_EPI
+    uint64_t *full = reinterpret_cast<uint64_t *>(epi_buf + (Cfg::TMA_EPI ? Cfg::EPI_BYTES : 0));
     uint64_t *empty = full + STAGES;
     uint64_t *sf_full = empty + STAGES;   // [STAGES] the stage's scales are in TMEM
     uint64_t *sf_data = sf_full + STAGES; // [STAGES] the stage's scale bytes are in smem
@@ -120,6 +121,7 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
         for (int g = 0; g < p.num_groups; ++g) {
             tma_prefetch_desc(&p.tma[g]);
             tma_prefetch_desc(&p.tmb[g]);
+            if (Cfg::TMA_EPI && p.prob[g].c_tma) tma_prefetch_desc(&p.tmc[g]);
         }
     }
     if (warp == 1) {
@@ -300,6 +302,8 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
         const int q = warp & 3;                  // TMEM lane quadrant of this warp
         const int row_in_tile = q * 32 + lane;
         const uint32_t t_row = tmem_acc + (static_cast<uint32_t>(q * 32) << 16);
+        uint8_t *wbuf = epi_buf + q * 4096;     // this warp's two staging buffers
+        int stores = 0;                         // TMA stores this warp has issued
         int ul = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++ul) {
             const Unit w = decode_unit(p, u);
@@ -352,7 +356,38 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
                 }
                 tc_fence_before();
                 mbar_arrive(acc_empty);
-                if (run && row < pr.m) {
+                if (Cfg::TMA_EPI && pr.c_tma) {
+                    // 32 x 32 sub-tiles (this warp's 32 rows) through the warp's two
+                    // staging buffers, written by TMA: each lane writes its row's 64
+                    // bytes in the 64-byte-swizzled layout of the tensor map (16-byte
+                    // chunk j of row r at chunk j ^ ((r / 2) % 4)); the map clips rows
+                    // past M and columns past N
+                    if (run) {
+#pragma unroll
+                        for (int c = 0; c < BN / 32; ++c) {
+                            const int col0 = w.n_tile * BN + c * 32;
+                            if (col0 < pr.n) {
+                                uint8_t *buf = wbuf + (stores & 1) * 2048;
+                                if (stores >= 2) {
+                                    if (lane == 0) bulk_wait_read<1>();   // the buffer's previous store has read it
+                                    __syncwarp();
+                                }
+#pragma unroll
+                                for (int j = 0; j < 4; ++j)
+                                    *reinterpret_cast<uint4 *>(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                                        make_uint4(pk[c * 16 + 4 * j], pk[c * 16 + 4 * j + 1], pk[c * 16 + 4 * j + 2],
+                                                   pk[c * 16 + 4 * j + 3]);
+                                fence_proxy_async_smem();
+                                __syncwarp();
+                                if (lane == 0) {
+                                    tma_store_2d(&p.tmc[w.g], buf, col0, w.m_tile * 128 + q * 32);
+                                    bulk_commit();
+                                }
+                                ++stores;
+                            }
+                        }
+                    }
+                } else if (run && row < pr.m) {
 #pragma unroll
                     for (int c = 0; c < BN / 32; ++c) {
                         const int col0 = w.n_tile * BN + c * 32;
@@ -418,6 +453,8 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
                 epilogue_bar();   // last_flag is reused by the next unit
             }
         }
+        // C stores by TMA have completed before the CTA leaves
+        if (Cfg::TMA_EPI && lane == 0) bulk_wait_all();
     }
     __syncwarp();
 
@@ -473,6 +510,7 @@ void fill_problem(GemmParams<MAXG> &P, int g, const GemmProblemHost &h, int bn, 
 {
     P.tma[g] = h.tma;
     P.tmb[g] = h.tmb;
+    P.tmc[g] = h.tmc;
     GemmProblemDev &d = P.prob[g];
     d.sfa = h.sfa;
     d.sfb = h.sfb;
@@ -489,6 +527,7 @@ void fill_problem(GemmParams<MAXG> &P, int g, const GemmProblemHost &h, int bn, 
     d.alpha = h.alpha;
     d.beta = h.beta;
     d.bias = static_cast<const uint16_t *>(h.bias);
+    d.c_tma = h.c_tma ? 1 : 0;
     tiles += d.m_tiles * d.n_tiles;
 }
 

@@ -22,12 +22,14 @@ struct GemmProblemDev {
     int epi;          // nonzero: C = alpha * acc + beta * C + bias[col]
     float alpha, beta;
     const uint16_t *bias;   // [n] in C's type, or null
+    int c_tma;        // single-CTA kernel: store C tiles by TMA (tmc of the params)
 };
 
 template <int MAXG>
 struct GemmParams {
     CUtensorMap tma[MAXG];
     CUtensorMap tmb[MAXG];
+    CUtensorMap tmc[MAXG];
     GemmProblemDev prob[MAXG];
     int num_groups;
     int total_tiles;
@@ -58,7 +60,11 @@ struct GemmCfg {
     static constexpr uint32_t SF_COLS = SF_COLS_A + SF_COLS_B;
     static constexpr uint32_t TMEM_COLS = pow2_cols(BN + STAGES * SF_COLS);
     static constexpr uint32_t BAR_BYTES = 512;
-    static constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+    // epilogue staging for TMA stores of C: two 2 KB buffers (32 x 32 16-bit
+    // values) per epilogue warp, where the stages leave room for them
+    static constexpr uint32_t EPI_BYTES = 4 * 2 * 2048;
+    static constexpr bool TMA_EPI = STAGES * STAGE_BYTES + BAR_BYTES + 1024 + EPI_BYTES <= 232448;
+    static constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + (TMA_EPI ? EPI_BYTES : 0) + BAR_BYTES + 1024;
     static_assert(STAGE_BYTES % 1024 == 0, "stage must keep 1024-byte alignment");
     static_assert(BN + STAGES * SF_COLS <= 512, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");

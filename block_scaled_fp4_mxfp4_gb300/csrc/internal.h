@@ -91,6 +91,10 @@ struct GemmProblemHost {
     // one stage's K-blocks (2 for MXFP4, 4 for NVFP4)
     CUtensorMap tmsfa;
     CUtensorMap tmsfb;
+    // single-CTA kernel: C as a 16-bit [m, n] tensor, box {32, 32}, 64-byte
+    // swizzle, for tiles stored by TMA (c_tma; else C is stored directly)
+    CUtensorMap tmc;
+    bool c_tma;
 };
 
 // Tile width along N of the grouped NVFP4 GEMM (box rows of tmb).
