@@ -7,6 +7,7 @@
 #include <cstring>
 #include <mutex>
 #include <unordered_map>
+#include <vector>
 
 #include "internal.h"
 #include "mxfp4.h"
@@ -333,13 +334,24 @@ mxfp4_status_t run_gemm(const void *Aq, int64_t ldaq, const void *A_sf, const vo
 
 // ------------------------------------------------------------ grouped GEMMs
 // nvfp4_group_gemm (E4M3 per 16, fp16 C) and mxfp4_group_gemm (E8M0 per 32,
-// bf16 C) share the validation, the tensor maps and the kernel choice.
+// bf16 C) share the validation, the tensor maps and the kernel choice. Up to
+// kMaxGroups problems travel in kernel parameters; longer lists in a device
+// table at the start of the caller's workspace.
+constexpr int kMaxGroupsAny = 1 << 20;   // sanity bound on a problem list's length
+
+size_t group_ws_bytes(int num_groups)
+{
+    return num_groups > kMaxGroups ? group_table_bytes(num_groups) : 0;
+}
+
+inline bool al64(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 63u) == 0; }
+
 template <typename Problem>
 mxfp4_status_t check_groups(const Problem *problems, int num_groups, int vec, bool pointers, int64_t *tiles,
                             int64_t *pair_tile_count)
 {
     if (!problems || num_groups < 1) return MXFP4_ERR_INVALID_ARG;
-    if (num_groups > kMaxGroups) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+    if (num_groups > kMaxGroupsAny) return MXFP4_ERR_UNSUPPORTED_SHAPE;
     const int bn = gemm_block_n_nv();
     *tiles = 0;
     *pair_tile_count = 0;
@@ -361,19 +373,27 @@ mxfp4_status_t check_groups(const Problem *problems, int num_groups, int vec, bo
     return MXFP4_OK;
 }
 
+// `table`: device memory of group_ws_bytes(num_groups) bytes (64-byte
+// aligned) for lists longer than kMaxGroups, else unused.
 template <typename Problem>
-mxfp4_status_t group_gemm(const Problem *problems, int num_groups, bool nv, void *stream)
+mxfp4_status_t group_gemm(const Problem *problems, int num_groups, bool nv, void *table, size_t table_bytes,
+                          void *stream)
 {
     const int vec = nv ? 16 : 32;
     int64_t tiles = 0, pair_tile_count = 0;
     mxfp4_status_t st = check_groups(problems, num_groups, vec, true, &tiles, &pair_tile_count);
     if (st != MXFP4_OK) return st;
+    if (num_groups > kMaxGroups) {
+        if (!table) return MXFP4_ERR_INVALID_ARG;
+        if (!al64(table)) return MXFP4_ERR_MISALIGNED;
+        if (table_bytes < group_ws_bytes(num_groups)) return MXFP4_ERR_WORKSPACE_TOO_SMALL;
+    }
     const bool pair = use_pair(pair_tile_count);
     int sms = 0;
     st = current_device(&sms);
     if (st != MXFP4_OK) return st;
-    GemmProblemHost hp[kMaxGroups];
-    memset(hp, 0, sizeof(hp));
+    std::vector<GemmProblemHost> hp(static_cast<size_t>(num_groups));
+    memset(hp.data(), 0, hp.size() * sizeof(GemmProblemHost));
     const int bn = gemm_block_n_nv();
     for (int g = 0; g < num_groups; ++g) {
         const Problem &p = problems[g];
@@ -403,10 +423,10 @@ mxfp4_status_t group_gemm(const Problem *problems, int num_groups, bool nv, void
     }
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (nv)
-        return cuda_status(pair ? launch_gemm_nv_grouped_pair(hp, num_groups, s)
-                                : launch_gemm_nv_grouped(hp, num_groups, s));
-    return cuda_status(pair ? launch_gemm_mx_grouped_pair(hp, num_groups, s)
-                            : launch_gemm_mx_grouped(hp, num_groups, s));
+        return cuda_status(pair ? launch_gemm_nv_grouped_pair(hp.data(), num_groups, table, s)
+                                : launch_gemm_nv_grouped(hp.data(), num_groups, table, s));
+    return cuda_status(pair ? launch_gemm_mx_grouped_pair(hp.data(), num_groups, table, s)
+                            : launch_gemm_mx_grouped(hp.data(), num_groups, table, s));
 }
 
 template <typename Problem>
@@ -432,18 +452,22 @@ mxfp4_status_t group_gemm_plan(const Problem *problems, int num_groups, bool nv,
 
 // nvfp4_group_quant_gemm: validation of the bf16 problem list and the
 // workspace layout (per group: packed A with 16-byte rows, then its scales,
-// each at a 256-byte offset).
+// each at a 256-byte offset; then, for lists longer than kMaxGroups, the
+// grouped GEMM's problem table).
 struct ActWorkspace {
-    size_t aq_off[kMaxGroups], sf_off[kMaxGroups];
-    int64_t ldq[kMaxGroups];
-    size_t total;
+    std::vector<size_t> aq_off, sf_off;
+    std::vector<int64_t> ldq;
+    size_t table_off, total;
 };
 
 mxfp4_status_t check_act_groups(const nvfp4_act_problem_t *problems, int num_groups, bool pointers,
                                 ActWorkspace *ws)
 {
     if (!problems || num_groups < 1) return MXFP4_ERR_INVALID_ARG;
-    if (num_groups > kMaxGroups) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+    if (num_groups > kMaxGroupsAny) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+    ws->aq_off.resize(num_groups);
+    ws->sf_off.resize(num_groups);
+    ws->ldq.resize(num_groups);
     size_t off = 0;
     for (int g = 0; g < num_groups; ++g) {
         const nvfp4_act_problem_t &p = problems[g];
@@ -462,7 +486,8 @@ mxfp4_status_t check_act_groups(const nvfp4_act_problem_t *problems, int num_gro
         ws->sf_off[g] = off;
         off += up256(sf_bytes(p.m, p.k, 16));
     }
-    ws->total = off;
+    ws->table_off = off;
+    ws->total = off + group_ws_bytes(num_groups);
     return MXFP4_OK;
 }
 
@@ -485,7 +510,7 @@ const char *mxfp4_status_string(mxfp4_status_t s)
     return "MXFP4_UNKNOWN_STATUS";
 }
 
-int mxfp4_abi_version(void) { return 1; }
+int mxfp4_abi_version(void) { return 2; }
 
 size_t mxfp4_sf_bytes(int64_t rows, int64_t k, int vec)
 {
@@ -501,8 +526,12 @@ size_t mxfp4_workspace_bytes(int64_t M, int64_t N, int64_t K)
 
 size_t nvfp4_group_workspace_bytes(int num_groups)
 {
-    (void)num_groups;
-    return 0;
+    return num_groups < 1 || num_groups > kMaxGroupsAny ? 0 : group_ws_bytes(num_groups);
+}
+
+size_t mxfp4_group_workspace_bytes(int num_groups)
+{
+    return num_groups < 1 || num_groups > kMaxGroupsAny ? 0 : group_ws_bytes(num_groups);
 }
 
 mxfp4_status_t mxfp4_quantize(const void *A, int64_t M, int64_t K, int64_t lda, void *Aq, int64_t ldq,
@@ -625,9 +654,7 @@ mxfp4_status_t nvfp4_quant_gemm_fused(const void *A, int64_t lda, const void *Bq
 mxfp4_status_t nvfp4_group_gemm(const nvfp4_problem_t *problems, int num_groups, void *workspace, size_t ws_bytes,
                                 void *stream)
 {
-    (void)workspace;
-    (void)ws_bytes;
-    return group_gemm(problems, num_groups, true, stream);
+    return group_gemm(problems, num_groups, true, workspace, ws_bytes, stream);
 }
 
 mxfp4_status_t mxfp4_rmsnorm_quantize(const void *X, int64_t M, int64_t K, int64_t ldx, const void *weight,
@@ -661,8 +688,8 @@ mxfp4_status_t nvfp4_group_quant_gemm(const nvfp4_act_problem_t *problems, int n
     if (!al16(workspace)) return MXFP4_ERR_MISALIGNED;
     if (ws_bytes < wl.total) return MXFP4_ERR_WORKSPACE_TOO_SMALL;
     uint8_t *w = static_cast<uint8_t *>(workspace);
-    nvfp4_problem_t q[kMaxGroups];
-    QuantGroupHost qg[kMaxGroups];
+    std::vector<nvfp4_problem_t> q(static_cast<size_t>(num_groups));
+    std::vector<QuantGroupHost> qg(static_cast<size_t>(num_groups));
     for (int g = 0; g < num_groups; ++g) {
         const nvfp4_act_problem_t &p = problems[g];
         q[g].m = p.m;
@@ -680,19 +707,25 @@ mxfp4_status_t nvfp4_group_quant_gemm(const nvfp4_act_problem_t *problems, int n
     }
     // the GEMM half's own checks, so that nothing is enqueued on a bad list
     int64_t tiles = 0, pair_tile_count = 0;
-    st = check_groups(q, num_groups, 16, true, &tiles, &pair_tile_count);
+    st = check_groups(q.data(), num_groups, 16, true, &tiles, &pair_tile_count);
     if (st != MXFP4_OK) return st;
+    if (num_groups > kMaxGroups && !al64(w + wl.table_off)) return MXFP4_ERR_MISALIGNED;
     int sms = 0;
     st = current_device(&sms);
     if (st != MXFP4_OK) return st;
-    st = cuda_status(launch_quant_nv_grouped(qg, num_groups, sms, static_cast<cudaStream_t>(stream)));
-    if (st != MXFP4_OK) return st;
-    return group_gemm(q, num_groups, true, stream);
+    // one quantization launch per kMaxGroups groups
+    for (int g0 = 0; g0 < num_groups; g0 += kMaxGroups) {
+        st = cuda_status(launch_quant_nv_grouped(qg.data() + g0, std::min(kMaxGroups, num_groups - g0), sms,
+                                                 static_cast<cudaStream_t>(stream)));
+        if (st != MXFP4_OK) return st;
+    }
+    return group_gemm(q.data(), num_groups, true, w + wl.table_off, ws_bytes - wl.table_off, stream);
 }
 
-mxfp4_status_t mxfp4_group_gemm(const mxfp4_problem_t *problems, int num_groups, void *stream)
+mxfp4_status_t mxfp4_group_gemm(const mxfp4_problem_t *problems, int num_groups, void *workspace, size_t ws_bytes,
+                                void *stream)
 {
-    return group_gemm(problems, num_groups, false, stream);
+    return group_gemm(problems, num_groups, false, workspace, ws_bytes, stream);
 }
 
 mxfp4_status_t mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, int which, mxfp4_plan_t *out)

@@ -28,7 +28,10 @@
 // Split-K (splits > 1): each split writes fp32 partials to the workspace; the
 // last split to arrive (atomic ticket) sums them in split order and writes C,
 // then resets its ticket so the workspace stays zeroed.
+#include <algorithm>
 #include <cstring>
+#include <mutex>
+#include <vector>
 
 #include "gemm_common.cuh"
 #include "internal.h"
@@ -49,17 +52,15 @@ struct Unit {
     int g, tile, m_tile, n_tile, split, s_begin, nst;
 };
 
-template <int MAXG>
-__device__ __forceinline__ Unit decode_unit(const GemmParams<MAXG> &p, int u)
+template <class P>
+__device__ __forceinline__ Unit decode_unit(const P &p, int u)
 {
     Unit w;
     w.tile = u % p.total_tiles;
     w.split = u / p.total_tiles;
-    int g = 0;
-#pragma unroll 1
-    while (g + 1 < p.num_groups && w.tile >= p.prob[g + 1].tile_start) ++g;
+    const int g = group_of_tile(p, w.tile);
     w.g = g;
-    const GemmProblemDev &pr = p.prob[g];
+    const GemmProblemDev &pr = p.problem(g);
     const int local = w.tile - pr.tile_start;
     w.m_tile = local % pr.m_tiles;
     w.n_tile = local / pr.m_tiles;
@@ -80,8 +81,10 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams<MAXG> &p, int u)
 //                  write C while the next unit's mainloop runs
 // EPI: the variant with the alpha / beta / bias epilogue (mxfp4_gemm_a4w4_ex);
 // the plain variant keeps its registers for the common case.
-template <int KIND, int BN, int STAGES, int MAXG, bool F16, bool EPI = false>
-__global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__ GemmParams<MAXG> p)
+// P: GemmParams<MAXG> (problems in kernel parameters) or GemmParamsTable
+// (problems in a device table).
+template <int KIND, int BN, int STAGES, class P, bool F16, bool EPI = false>
+__global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__ P p)
 {
     using Cfg = GemmCfg<KIND, BN, STAGES>;
     constexpr bool MX = Cfg::MX;
@@ -118,10 +121,11 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
         mbar_init(cp_done + 1, 1);
         *abort_flag = 0;
         fence_mbar_init();
-        for (int g = 0; g < p.num_groups; ++g) {
-            tma_prefetch_desc(&p.tma[g]);
-            tma_prefetch_desc(&p.tmb[g]);
-            if (Cfg::TMA_EPI && p.prob[g].c_tma) tma_prefetch_desc(&p.tmc[g]);
+        // a device table's maps are fetched when first used, below
+        for (int g = 0; g < (P::kTable ? 0 : p.num_groups); ++g) {
+            tma_prefetch_desc(p.map_a(g));
+            tma_prefetch_desc(p.map_b(g));
+            if (Cfg::TMA_EPI && p.problem(g).c_tma) tma_prefetch_desc(p.map_c(g));
         }
     }
     if (warp == 1) {
@@ -143,10 +147,15 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
         if (lane == 0) {
             // ------------------------------------------------------ TMA producer
             const uint64_t pol = policy_evict_last();
-            int gs = 0;
+            int gs = 0, g_seen = -1;
             for (int u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
                 const Unit w = decode_unit(p, u);
-                const GemmProblemDev &pr = p.prob[w.g];
+                const GemmProblemDev &pr = p.problem(w.g);
+                if (P::kTable && w.g != g_seen) {
+                    tma_desc_acquire(p.map_a(w.g));
+                    tma_desc_acquire(p.map_b(w.g));
+                    g_seen = w.g;
+                }
                 int nch_valid = 0;
 #pragma unroll
                 for (int j = 0; j < Cfg::NCH; ++j)
@@ -173,8 +182,8 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
                                   pr.sfb + (static_cast<size_t>(w.n_tile * Cfg::NCH + j) * pr.sf_cblocks + blk0) * 512,
                                   nblk * 512, sf_data + slot, pol);
                     mbar_arrive_expect_tx(full + slot, Cfg::A_BYTES + Cfg::B_BYTES);
-                    tma_load_2d(st, &p.tma[w.g], ks * 128, w.m_tile * 128, full + slot, pol);
-                    tma_load_2d(st + Cfg::A_BYTES, &p.tmb[w.g], ks * 128, w.n_tile * BN, full + slot, pol);
+                    tma_load_2d(st, p.map_a(w.g), ks * 128, w.m_tile * 128, full + slot, pol);
+                    tma_load_2d(st + Cfg::A_BYTES, p.map_b(w.g), ks * 128, w.n_tile * BN, full + slot, pol);
                     issued = gs + 1;
                 }
             }
@@ -187,7 +196,7 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
         int gs = 0, ul = 0, commits = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++ul) {
             const Unit w = decode_unit(p, u);
-            const GemmProblemDev &pr = p.prob[w.g];
+            const GemmProblemDev &pr = p.problem(w.g);
             const int k_steps_total = (pr.k + 63) / 64;
             if (ul > 0 && !mbar_wait(acc_empty, (ul - 1) & 1, &g_gemm_error, kErrWaitAccum, p.wait_ns)) {
                 *abort_flag = 1;
@@ -258,7 +267,7 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
             bool stop = false;
             for (int u = blockIdx.x; u < units && !stop && !*abort_flag; u += gridDim.x) {
                 const Unit w = decode_unit(p, u);
-                const GemmProblemDev &pr = p.prob[w.g];
+                const GemmProblemDev &pr = p.problem(w.g);
                 const int k_steps_total = (pr.k + 63) / 64;
                 for (int i = 0; i < w.nst; ++i, ++gs) {
                     const int slot = gs % STAGES;
@@ -307,7 +316,7 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
         int ul = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++ul) {
             const Unit w = decode_unit(p, u);
-            const GemmProblemDev &pr = p.prob[w.g];
+            const GemmProblemDev &pr = p.problem(w.g);
             // one thread waits and decides for all four warps, so that they
             // leave the loop together (the split-K path has named barriers)
             if (threadIdx.x == 128) {
@@ -380,7 +389,8 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
                                 fence_proxy_async_smem();
                                 __syncwarp();
                                 if (lane == 0) {
-                                    tma_store_2d(&p.tmc[w.g], buf, col0, w.m_tile * 128 + q * 32);
+                                    if (P::kTable && c == 0) tma_desc_acquire(p.map_c(w.g));
+                                    tma_store_2d(p.map_c(w.g), buf, col0, w.m_tile * 128 + q * 32);
                                     bulk_commit();
                                 }
                                 ++stores;
@@ -474,11 +484,11 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
     }
 }
 
-template <int KIND, int BN, int STAGES, int MAXG, bool F16, bool EPI = false>
-cudaError_t launch_bs_gemm(const GemmParams<MAXG> &params, cudaStream_t stream)
+template <int KIND, int BN, int STAGES, class P, bool F16, bool EPI = false>
+cudaError_t launch_bs_gemm(const P &params, cudaStream_t stream)
 {
     using Cfg = GemmCfg<KIND, BN, STAGES>;
-    auto kern = bs_gemm_kernel<KIND, BN, STAGES, MAXG, F16, EPI>;
+    auto kern = bs_gemm_kernel<KIND, BN, STAGES, P, F16, EPI>;
     static KernelOnce once;
     int sms = 0;
     const cudaError_t e = prepare_kernel(kern, Cfg::SMEM_BYTES, once, &sms);
@@ -496,9 +506,9 @@ cudaError_t launch_bs_gemm(const GemmParams<MAXG> &params, cudaStream_t stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    GemmParams<MAXG> P = params;
-    P.wait_ns = wait_limit_ns();
-    return cudaLaunchKernelEx(&cfg, kern, P);
+    P launch_params = params;
+    launch_params.wait_ns = wait_limit_ns();
+    return cudaLaunchKernelEx(&cfg, kern, launch_params);
 }
 
 constexpr int kMxStages = 4;        // BN = 256
@@ -549,39 +559,101 @@ cudaError_t launch_gemm_mx(const GemmProblemHost &prob, int bn, int splits, floa
     P.partials = partials;
     P.tickets = tickets;
     if (prob.epi) {
-        if (bn == 128) return launch_bs_gemm<0, 128, kMxNarrowStages, 1, false, true>(P, stream);
-        return launch_bs_gemm<0, 256, kMxStages, 1, false, true>(P, stream);
+        if (bn == 128) return launch_bs_gemm<0, 128, kMxNarrowStages, GemmParams<1>, false, true>(P, stream);
+        return launch_bs_gemm<0, 256, kMxStages, GemmParams<1>, false, true>(P, stream);
     }
-    if (bn == 128) return launch_bs_gemm<0, 128, kMxNarrowStages, 1, false>(P, stream);
-    return launch_bs_gemm<0, 256, kMxStages, 1, false>(P, stream);
+    if (bn == 128) return launch_bs_gemm<0, 128, kMxNarrowStages, GemmParams<1>, false>(P, stream);
+    return launch_bs_gemm<0, 256, kMxStages, GemmParams<1>, false>(P, stream);
 }
 
-cudaError_t launch_gemm_nv_grouped(const GemmProblemHost *probs, int num_groups, cudaStream_t stream)
+// The grouped launch: problems in kernel parameters up to kMaxGroups, else in
+// the device table (filled here, on the stream, before the launch).
+template <int KIND, int BN, int STAGES, bool F16>
+cudaError_t launch_grouped(const GemmProblemHost *probs, int num_groups, void *table, int vec, cudaStream_t stream)
 {
-    GemmParams<kMaxGroups> P;
-    memset(&P, 0, sizeof(P));
+    if (num_groups <= kMaxGroups) {
+        GemmParams<kMaxGroups> P;
+        memset(&P, 0, sizeof(P));
+        int tiles = 0;
+        for (int g = 0; g < num_groups; ++g) fill_problem(P, g, probs[g], BN, vec, tiles);
+        P.num_groups = num_groups;
+        P.total_tiles = tiles;
+        P.splits = 1;
+        return launch_bs_gemm<KIND, BN, STAGES, GemmParams<kMaxGroups>, F16>(P, stream);
+    }
+    if (!table || (reinterpret_cast<uintptr_t>(table) & 63u) != 0) return cudaErrorInvalidValue;
+    std::vector<uint8_t> host(group_table_bytes(num_groups), 0);
+    CUtensorMap *maps = reinterpret_cast<CUtensorMap *>(host.data());
+    uint8_t *recs = host.data() + static_cast<size_t>(num_groups) * kTableMaps * sizeof(CUtensorMap);
+    GemmParams<1> one;
     int tiles = 0;
-    for (int g = 0; g < num_groups; ++g) fill_problem(P, g, probs[g], kNvBN, 16, tiles);
-    P.num_groups = num_groups;
-    P.total_tiles = tiles;
-    P.splits = 1;
-    P.partials = nullptr;
-    P.tickets = nullptr;
-    return launch_bs_gemm<1, kNvBN, kNvStages, kMaxGroups, true>(P, stream);
+    for (int g = 0; g < num_groups; ++g) {
+        memset(&one, 0, sizeof(one));
+        int t = tiles;
+        fill_problem(one, 0, probs[g], BN, vec, t);
+        one.prob[0].tile_start = tiles;
+        tiles = t;
+        maps[g * kTableMaps + 0] = probs[g].tma;
+        maps[g * kTableMaps + 1] = probs[g].tmb;
+        maps[g * kTableMaps + 2] = probs[g].tmc;
+        memcpy(recs + static_cast<size_t>(g) * kTableProblemBytes, &one.prob[0], sizeof(GemmProblemDev));
+    }
+    cudaError_t e = upload_table(table, host.data(), host.size(), stream);
+    if (e != cudaSuccess) return e;
+    GemmParamsTable T;
+    memset(&T, 0, sizeof(T));
+    T.maps = static_cast<const CUtensorMap *>(table);
+    T.probs = static_cast<const uint8_t *>(table) + static_cast<size_t>(num_groups) * kTableMaps * sizeof(CUtensorMap);
+    T.num_groups = num_groups;
+    T.total_tiles = tiles;
+    T.splits = 1;
+    return launch_bs_gemm<KIND, BN, STAGES, GemmParamsTable, F16>(T, stream);
 }
 
-cudaError_t launch_gemm_mx_grouped(const GemmProblemHost *probs, int num_groups, cudaStream_t stream)
+cudaError_t launch_gemm_nv_grouped(const GemmProblemHost *probs, int num_groups, void *table, cudaStream_t stream)
 {
-    GemmParams<kMaxGroups> P;
-    memset(&P, 0, sizeof(P));
-    int tiles = 0;
-    for (int g = 0; g < num_groups; ++g) fill_problem(P, g, probs[g], kNvBN, 32, tiles);
-    P.num_groups = num_groups;
-    P.total_tiles = tiles;
-    P.splits = 1;
-    P.partials = nullptr;
-    P.tickets = nullptr;
-    return launch_bs_gemm<0, kNvBN, kMxStages, kMaxGroups, false>(P, stream);
+    return launch_grouped<1, kNvBN, kNvStages, true>(probs, num_groups, table, 16, stream);
+}
+
+cudaError_t launch_gemm_mx_grouped(const GemmProblemHost *probs, int num_groups, void *table, cudaStream_t stream)
+{
+    return launch_grouped<0, kNvBN, kMxStages, false>(probs, num_groups, table, 32, stream);
+}
+
+namespace {
+
+constexpr int kUploadChunk = 30720;   // table bytes per upload launch (kernel parameters)
+
+struct UploadChunk {
+    uint4 *dst;
+    uint32_t n16;                      // 16-byte words to copy
+    uint32_t pad_;
+    uint4 data[kUploadChunk / 16];
+};
+
+__global__ void __launch_bounds__(256) table_upload_kernel(const __grid_constant__ UploadChunk c)
+{
+    for (uint32_t i = threadIdx.x; i < c.n16; i += blockDim.x) c.dst[i] = c.data[i];
+}
+
+}  // namespace
+
+cudaError_t upload_table(void *dst, const void *src, size_t bytes, cudaStream_t stream)
+{
+    if ((reinterpret_cast<uintptr_t>(dst) & 15u) != 0 || bytes % 16 != 0) return cudaErrorInvalidValue;
+    static UploadChunk c;   // host staging of one launch's parameters (copied at launch)
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lk(mu);
+    for (size_t off = 0; off < bytes; off += kUploadChunk) {
+        const size_t n = std::min(bytes - off, static_cast<size_t>(kUploadChunk));
+        c.dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(dst) + off);
+        c.n16 = static_cast<uint32_t>(n / 16);
+        memcpy(c.data, static_cast<const uint8_t *>(src) + off, n);
+        table_upload_kernel<<<1, 256, 0, stream>>>(c);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 int read_and_clear_gemm_error()

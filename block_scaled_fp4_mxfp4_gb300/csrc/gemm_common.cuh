@@ -25,6 +25,9 @@ struct GemmProblemDev {
     int c_tma;        // single-CTA kernel: store C tiles by TMA (tmc of the params)
 };
 
+static_assert(sizeof(GemmProblemDev) <= kTableProblemBytes, "problem record of the device table");
+
+// The problems of a launch in kernel parameters (up to MAXG of them).
 template <int MAXG>
 struct GemmParams {
     CUtensorMap tma[MAXG];
@@ -38,7 +41,60 @@ struct GemmParams {
     float *partials;
     int *tickets;
     uint64_t wait_ns;   // limit of the waits that guard work
+    static constexpr bool kTable = false;
+    __device__ __forceinline__ const CUtensorMap *map_a(int g) const { return &tma[g]; }
+    __device__ __forceinline__ const CUtensorMap *map_b(int g) const { return &tmb[g]; }
+    __device__ __forceinline__ const CUtensorMap *map_c(int g) const { return &tmc[g]; }
+    __device__ __forceinline__ const GemmProblemDev &problem(int g) const { return prob[g]; }
 };
+
+// The problems of a launch in a table in global memory (any number of them):
+// per group four tensor maps (A, B, C) then its problem record, laid out as
+// group_table_bytes() describes.
+struct GemmParamsTable {
+    const CUtensorMap *maps;      // [num_groups][kTableMaps]
+    const uint8_t *probs;         // [num_groups][kTableProblemBytes]
+    int num_groups;
+    int total_tiles;
+    int splits;
+    int pad_;
+    float *partials;
+    int *tickets;
+    uint64_t wait_ns;
+    static constexpr bool kTable = true;
+    __device__ __forceinline__ const CUtensorMap *map_a(int g) const { return maps + g * kTableMaps; }
+    __device__ __forceinline__ const CUtensorMap *map_b(int g) const { return maps + g * kTableMaps + 1; }
+    __device__ __forceinline__ const CUtensorMap *map_c(int g) const { return maps + g * kTableMaps + 2; }
+    __device__ __forceinline__ const GemmProblemDev &problem(int g) const
+    {
+        return *reinterpret_cast<const GemmProblemDev *>(probs + static_cast<size_t>(g) * kTableProblemBytes);
+    }
+};
+
+// Group of linear tile `tile`: the last problem whose first tile is <= tile
+// (first tiles strictly increase). A short scan for parameter tables, a
+// binary search for device tables of any length.
+template <class P>
+__device__ __forceinline__ int group_of_tile(const P &p, int tile)
+{
+    if constexpr (!P::kTable) {
+        int g = 0;
+#pragma unroll 1
+        while (g + 1 < p.num_groups && tile >= p.problem(g + 1).tile_start) ++g;
+        return g;
+    } else {
+        int lo = 0, hi = p.num_groups - 1;
+#pragma unroll 1
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.problem(mid).tile_start <= tile)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        return lo;
+    }
+}
 
 __host__ __device__ constexpr uint32_t pow2_cols(uint32_t n)
 {

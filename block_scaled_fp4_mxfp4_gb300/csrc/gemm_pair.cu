@@ -30,6 +30,7 @@
 // until neither can touch the other's shared memory, then the pair frees its
 // TMEM together.
 #include <cstring>
+#include <vector>
 
 #include "gemm_common.cuh"
 #include "internal.h"
@@ -70,6 +71,7 @@ constexpr int kPairEpiWarps = 8;
 
 __device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
+// The problems of a launch in kernel parameters (up to MAXG of them).
 template <int MAXG>
 struct PairParams {
     CUtensorMap tma[MAXG];     // packed A, box {128 B, 128 rows}
@@ -80,6 +82,31 @@ struct PairParams {
     int num_groups;
     int total_tiles;
     uint64_t wait_ns;          // limit of the waits that guard work
+    static constexpr bool kTable = false;
+    __device__ __forceinline__ const CUtensorMap *map_a(int g) const { return &tma[g]; }
+    __device__ __forceinline__ const CUtensorMap *map_b(int g) const { return &tmb[g]; }
+    __device__ __forceinline__ const CUtensorMap *map_sfa(int g) const { return &tmsfa[g]; }
+    __device__ __forceinline__ const CUtensorMap *map_sfb(int g) const { return &tmsfb[g]; }
+    __device__ __forceinline__ const GemmProblemDev &problem(int g) const { return prob[g]; }
+};
+
+// The problems of a launch in a device table (any number): per group the
+// maps A, B, A scales, B scales, then the problem record.
+struct PairParamsTable {
+    const CUtensorMap *maps;   // [num_groups][kTableMaps]
+    const uint8_t *probs;      // [num_groups][kTableProblemBytes]
+    int num_groups;
+    int total_tiles;
+    uint64_t wait_ns;
+    static constexpr bool kTable = true;
+    __device__ __forceinline__ const CUtensorMap *map_a(int g) const { return maps + g * kTableMaps; }
+    __device__ __forceinline__ const CUtensorMap *map_b(int g) const { return maps + g * kTableMaps + 1; }
+    __device__ __forceinline__ const CUtensorMap *map_sfa(int g) const { return maps + g * kTableMaps + 2; }
+    __device__ __forceinline__ const CUtensorMap *map_sfb(int g) const { return maps + g * kTableMaps + 3; }
+    __device__ __forceinline__ const GemmProblemDev &problem(int g) const
+    {
+        return *reinterpret_cast<const GemmProblemDev *>(probs + static_cast<size_t>(g) * kTableProblemBytes);
+    }
 };
 
 struct PairUnit {
@@ -87,15 +114,13 @@ struct PairUnit {
 };
 
 // Pair tiles are numbered group by group, 256-row tiles fastest.
-template <int MAXG>
-__device__ __forceinline__ PairUnit decode_pair_unit(const PairParams<MAXG> &p, int u)
+template <class P>
+__device__ __forceinline__ PairUnit decode_pair_unit(const P &p, int u)
 {
     PairUnit w;
-    int g = 0;
-#pragma unroll 1
-    while (g + 1 < p.num_groups && u >= p.prob[g + 1].tile_start) ++g;
+    const int g = group_of_tile(p, u);
     w.g = g;
-    const GemmProblemDev &pr = p.prob[g];
+    const GemmProblemDev &pr = p.problem(g);
     const int local = u - pr.tile_start;
     w.m_pair = local % pr.m_tiles;
     w.n_tile = local / pr.m_tiles;
@@ -103,8 +128,9 @@ __device__ __forceinline__ PairUnit decode_pair_unit(const PairParams<MAXG> &p, 
 }
 
 // EPI: the variant with the alpha / beta / bias epilogue (mxfp4_gemm_a4w4_ex).
-template <int KIND, int STAGES, int MAXG, bool F16, bool EPI = false>
-__global__ void __launch_bounds__(kPairThreads, 1) bs_gemm_pair_kernel(const __grid_constant__ PairParams<MAXG> p)
+// P: PairParams<MAXG> (problems in kernel parameters) or PairParamsTable.
+template <int KIND, int STAGES, class P, bool F16, bool EPI = false>
+__global__ void __launch_bounds__(kPairThreads, 1) bs_gemm_pair_kernel(const __grid_constant__ P p)
 {
     using Cfg = PairCfg<KIND, STAGES>;
     constexpr bool MX = Cfg::MX;
@@ -144,11 +170,12 @@ __global__ void __launch_bounds__(kPairThreads, 1) bs_gemm_pair_kernel(const __g
         mbar_init(cp_done + 1, 1);
         *abort_flag = 0;
         fence_mbar_init();
-        for (int g = 0; g < p.num_groups; ++g) {
-            tma_prefetch_desc(&p.tma[g]);
-            tma_prefetch_desc(&p.tmb[g]);
-            tma_prefetch_desc(&p.tmsfa[g]);
-            tma_prefetch_desc(&p.tmsfb[g]);
+        // a device table's maps are fetched when first used, below
+        for (int g = 0; g < (P::kTable ? 0 : p.num_groups); ++g) {
+            tma_prefetch_desc(p.map_a(g));
+            tma_prefetch_desc(p.map_b(g));
+            tma_prefetch_desc(p.map_sfa(g));
+            tma_prefetch_desc(p.map_sfb(g));
         }
     }
     if (warp == 1) {
@@ -179,10 +206,17 @@ __global__ void __launch_bounds__(kPairThreads, 1) bs_gemm_pair_kernel(const __g
             const uint64_t pol = policy_evict_last();
             const uint32_t full_r0 = mapa_shared(smem_u32(full), 0);
             const uint32_t sf_r0 = mapa_shared(smem_u32(sf_data), 0);
-            int gs = 0;
+            int gs = 0, g_seen = -1;
             for (int u = pair; u < units && !*abort_flag; u += npairs) {
                 const PairUnit w = decode_pair_unit(p, u);
-                const GemmProblemDev &pr = p.prob[w.g];
+                const GemmProblemDev &pr = p.problem(w.g);
+                if (P::kTable && w.g != g_seen) {
+                    tma_desc_acquire(p.map_a(w.g));
+                    tma_desc_acquire(p.map_b(w.g));
+                    tma_desc_acquire(p.map_sfa(w.g));
+                    tma_desc_acquire(p.map_sfb(w.g));
+                    g_seen = w.g;
+                }
                 const int a_chunk = w.m_pair * 2 + static_cast<int>(rank);   // this CTA's 128 rows of A
                 const int k_stages = (pr.k + 255) / 256;
                 for (int i = 0; i < k_stages; ++i, ++gs) {
@@ -199,15 +233,15 @@ __global__ void __launch_bounds__(kPairThreads, 1) bs_gemm_pair_kernel(const __g
                         mbar_arrive_expect_tx(full + slot, 2 * (Cfg::A_BYTES + Cfg::B_BYTES));
                     }
                     // the scale blocks first, on their own barrier
-                    tma_load_2d_pair(st + Cfg::A_BYTES + Cfg::B_BYTES, &p.tmsfa[w.g], 0, a_chunk * pr.sf_cblocks + blk0,
+                    tma_load_2d_pair(st + Cfg::A_BYTES + Cfg::B_BYTES, p.map_sfa(w.g), 0, a_chunk * pr.sf_cblocks + blk0,
                                      sf_r0 + slot * 8, pol);
 #pragma unroll
                     for (int j = 0; j < 2; ++j)
                         tma_load_2d_pair(st + Cfg::A_BYTES + Cfg::B_BYTES + Cfg::SFA_BYTES + j * Cfg::SF_BLK * 512,
-                                         &p.tmsfb[w.g], 0, (w.n_tile * 2 + j) * pr.sf_cblocks + blk0, sf_r0 + slot * 8,
+                                         p.map_sfb(w.g), 0, (w.n_tile * 2 + j) * pr.sf_cblocks + blk0, sf_r0 + slot * 8,
                                          pol);
-                    tma_load_2d_pair(st, &p.tma[w.g], i * 128, a_chunk * 128, full_r0 + slot * 8, pol);
-                    tma_load_2d_pair(st + Cfg::A_BYTES, &p.tmb[w.g], i * 128,
+                    tma_load_2d_pair(st, p.map_a(w.g), i * 128, a_chunk * 128, full_r0 + slot * 8, pol);
+                    tma_load_2d_pair(st + Cfg::A_BYTES, p.map_b(w.g), i * 128,
                                      w.n_tile * 256 + static_cast<int>(rank) * 128, full_r0 + slot * 8, pol);
                     issued = gs + 1;
                 }
@@ -220,7 +254,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) bs_gemm_pair_kernel(const __g
             int gs = 0, ul = 0, commits = 0;
             for (int u = pair; u < units; u += npairs, ++ul) {
                 const PairUnit w = decode_pair_unit(p, u);
-                const GemmProblemDev &pr = p.prob[w.g];
+                const GemmProblemDev &pr = p.problem(w.g);
                 const int k_stages = (pr.k + 255) / 256;
                 const int k_steps_total = (pr.k + 63) / 64;
                 // the epilogues' arrivals are relaxed: they publish no data, only
@@ -293,7 +327,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) bs_gemm_pair_kernel(const __g
             bool stop = false;
             for (int u = pair; u < units && !stop && !*abort_flag; u += npairs) {
                 const PairUnit w = decode_pair_unit(p, u);
-                const GemmProblemDev &pr = p.prob[w.g];
+                const GemmProblemDev &pr = p.problem(w.g);
                 const int k_stages = (pr.k + 255) / 256;
                 const int k_steps_total = (pr.k + 63) / 64;
                 for (int i = 0; i < k_stages; ++i, ++gs) {
@@ -348,7 +382,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) bs_gemm_pair_kernel(const __g
         int ul = 0;
         for (int u = pair; u < units; u += npairs, ++ul) {
             const PairUnit w = decode_pair_unit(p, u);
-            const GemmProblemDev &pr = p.prob[w.g];
+            const GemmProblemDev &pr = p.problem(w.g);
             // one thread waits and decides for the eight warps, so that they
             // leave the loop together
             if (threadIdx.x == 128) {
@@ -461,11 +495,11 @@ __global__ void __launch_bounds__(kPairThreads, 1) bs_gemm_pair_kernel(const __g
     }
 }
 
-template <int KIND, int STAGES, int MAXG, bool F16, bool EPI = false>
-cudaError_t launch_pair(const PairParams<MAXG> &params, cudaStream_t stream)
+template <int KIND, int STAGES, class P, bool F16, bool EPI = false>
+cudaError_t launch_pair(const P &params, cudaStream_t stream)
 {
     using Cfg = PairCfg<KIND, STAGES>;
-    auto kern = bs_gemm_pair_kernel<KIND, STAGES, MAXG, F16, EPI>;
+    auto kern = bs_gemm_pair_kernel<KIND, STAGES, P, F16, EPI>;
     static KernelOnce once;
     int sms = 0;
     const cudaError_t e = prepare_kernel(kern, Cfg::SMEM_BYTES, once, &sms);
@@ -486,9 +520,9 @@ cudaError_t launch_pair(const PairParams<MAXG> &params, cudaStream_t stream)
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    PairParams<MAXG> P = params;
-    P.wait_ns = wait_limit_ns();
-    return cudaLaunchKernelEx(&cfg, kern, P);
+    P launch_params = params;
+    launch_params.wait_ns = wait_limit_ns();
+    return cudaLaunchKernelEx(&cfg, kern, launch_params);
 }
 
 constexpr int kPairMxStages = 6;   // 35 KB stages
@@ -536,30 +570,64 @@ cudaError_t launch_gemm_mx_pair(const GemmProblemHost &prob, cudaStream_t stream
     fill_pair_problem(P, 0, prob, 32, tiles);
     P.num_groups = 1;
     P.total_tiles = tiles;
-    if (prob.epi) return launch_pair<0, kPairMxStages, 1, false, true>(P, stream);
-    return launch_pair<0, kPairMxStages, 1, false>(P, stream);
+    if (prob.epi) return launch_pair<0, kPairMxStages, PairParams<1>, false, true>(P, stream);
+    return launch_pair<0, kPairMxStages, PairParams<1>, false>(P, stream);
 }
 
-cudaError_t launch_gemm_nv_grouped_pair(const GemmProblemHost *probs, int num_groups, cudaStream_t stream)
+// The grouped launch: problems in kernel parameters up to kMaxGroups, else in
+// the device table (filled here, on the stream, before the launch).
+template <int KIND, int STAGES, bool F16>
+cudaError_t launch_grouped_pair(const GemmProblemHost *probs, int num_groups, void *table, int vec,
+                                cudaStream_t stream)
 {
-    PairParams<kMaxGroups> P;
-    memset(&P, 0, sizeof(P));
+    if (num_groups <= kMaxGroups) {
+        PairParams<kMaxGroups> P;
+        memset(&P, 0, sizeof(P));
+        int tiles = 0;
+        for (int g = 0; g < num_groups; ++g) fill_pair_problem(P, g, probs[g], vec, tiles);
+        P.num_groups = num_groups;
+        P.total_tiles = tiles;
+        return launch_pair<KIND, STAGES, PairParams<kMaxGroups>, F16>(P, stream);
+    }
+    if (!table || (reinterpret_cast<uintptr_t>(table) & 63u) != 0) return cudaErrorInvalidValue;
+    std::vector<uint8_t> host(group_table_bytes(num_groups), 0);
+    CUtensorMap *maps = reinterpret_cast<CUtensorMap *>(host.data());
+    uint8_t *recs = host.data() + static_cast<size_t>(num_groups) * kTableMaps * sizeof(CUtensorMap);
+    PairParams<1> one;
     int tiles = 0;
-    for (int g = 0; g < num_groups; ++g) fill_pair_problem(P, g, probs[g], 16, tiles);
-    P.num_groups = num_groups;
-    P.total_tiles = tiles;
-    return launch_pair<1, kPairNvStages, kMaxGroups, true>(P, stream);
+    for (int g = 0; g < num_groups; ++g) {
+        memset(&one, 0, sizeof(one));
+        int t = tiles;
+        fill_pair_problem(one, 0, probs[g], vec, t);
+        one.prob[0].tile_start = tiles;
+        tiles = t;
+        maps[g * kTableMaps + 0] = probs[g].tma;
+        maps[g * kTableMaps + 1] = probs[g].tmb;
+        maps[g * kTableMaps + 2] = probs[g].tmsfa;
+        maps[g * kTableMaps + 3] = probs[g].tmsfb;
+        memcpy(recs + static_cast<size_t>(g) * kTableProblemBytes, &one.prob[0], sizeof(GemmProblemDev));
+    }
+    cudaError_t e = upload_table(table, host.data(), host.size(), stream);
+    if (e != cudaSuccess) return e;
+    PairParamsTable T;
+    memset(&T, 0, sizeof(T));
+    T.maps = static_cast<const CUtensorMap *>(table);
+    T.probs = static_cast<const uint8_t *>(table) + static_cast<size_t>(num_groups) * kTableMaps * sizeof(CUtensorMap);
+    T.num_groups = num_groups;
+    T.total_tiles = tiles;
+    return launch_pair<KIND, STAGES, PairParamsTable, F16>(T, stream);
 }
 
-cudaError_t launch_gemm_mx_grouped_pair(const GemmProblemHost *probs, int num_groups, cudaStream_t stream)
+cudaError_t launch_gemm_nv_grouped_pair(const GemmProblemHost *probs, int num_groups, void *table,
+                                        cudaStream_t stream)
 {
-    PairParams<kMaxGroups> P;
-    memset(&P, 0, sizeof(P));
-    int tiles = 0;
-    for (int g = 0; g < num_groups; ++g) fill_pair_problem(P, g, probs[g], 32, tiles);
-    P.num_groups = num_groups;
-    P.total_tiles = tiles;
-    return launch_pair<0, kPairMxStages, kMaxGroups, false>(P, stream);
+    return launch_grouped_pair<1, kPairNvStages, true>(probs, num_groups, table, 16, stream);
+}
+
+cudaError_t launch_gemm_mx_grouped_pair(const GemmProblemHost *probs, int num_groups, void *table,
+                                        cudaStream_t stream)
+{
+    return launch_grouped_pair<0, kPairMxStages, false>(probs, num_groups, table, 32, stream);
 }
 
 int read_and_clear_gemm_pair_error()

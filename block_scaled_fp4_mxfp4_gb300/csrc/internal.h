@@ -10,7 +10,19 @@
 
 namespace mxfp4 {
 
+// Problems a grouped launch carries in its kernel parameters; longer lists
+// go through a table in the caller's workspace.
 constexpr int kMaxGroups = 16;
+
+// Device problem table: per group kTableMaps tensor maps (A, B, then C for the
+// single-CTA kernel or A scales, B scales for the CTA-pair kernel) and one
+// problem record of kTableProblemBytes.
+constexpr int kTableMaps = 4;
+constexpr size_t kTableProblemBytes = 128;
+constexpr size_t group_table_bytes(int num_groups)
+{
+    return static_cast<size_t>(num_groups) * (kTableMaps * sizeof(CUtensorMap) + kTableProblemBytes);
+}
 
 // Default limit of every bounded wait in the kernels (2 s of %globaltimer).
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
@@ -105,11 +117,13 @@ int gemm_block_n_nv();
 // floats) and zeroed `tickets` (one int per tile).
 cudaError_t launch_gemm_mx(const GemmProblemHost &prob, int bn, int splits, float *partials,
                            int *tickets, cudaStream_t stream);
-// Grouped NVFP4 (kind::mxf4nvf4, fp16 C), one launch over all groups.
-cudaError_t launch_gemm_nv_grouped(const GemmProblemHost *probs, int num_groups,
+// Grouped NVFP4 (kind::mxf4nvf4, fp16 C), one launch over all groups. More
+// than kMaxGroups problems need `table`: group_table_bytes(num_groups) bytes
+// of device memory (64-byte aligned), filled on `stream` before the launch.
+cudaError_t launch_gemm_nv_grouped(const GemmProblemHost *probs, int num_groups, void *table,
                                    cudaStream_t stream);
-// Grouped MXFP4 (kind::mxf4, bf16 C), one launch over all groups.
-cudaError_t launch_gemm_mx_grouped(const GemmProblemHost *probs, int num_groups,
+// Grouped MXFP4 (kind::mxf4, bf16 C), one launch over all groups; `table` as above.
+cudaError_t launch_gemm_mx_grouped(const GemmProblemHost *probs, int num_groups, void *table,
                                    cudaStream_t stream);
 int read_and_clear_gemm_error();
 
@@ -121,10 +135,16 @@ int pair_tiles(int64_t m, int64_t n);   // 256 x 256 tiles of an m x n output
 // scale blocks per tmsfa / tmsfb box (one stage): 2 for MXFP4, 4 for NVFP4
 constexpr int pair_sf_box_blocks(bool nvfp4) { return nvfp4 ? 4 : 2; }
 cudaError_t launch_gemm_mx_pair(const GemmProblemHost &prob, cudaStream_t stream);
-cudaError_t launch_gemm_nv_grouped_pair(const GemmProblemHost *probs, int num_groups,
+cudaError_t launch_gemm_nv_grouped_pair(const GemmProblemHost *probs, int num_groups, void *table,
                                         cudaStream_t stream);
-cudaError_t launch_gemm_mx_grouped_pair(const GemmProblemHost *probs, int num_groups,
+cudaError_t launch_gemm_mx_grouped_pair(const GemmProblemHost *probs, int num_groups, void *table,
                                         cudaStream_t stream);
+
+// Copies `bytes` (a multiple of 16) from host memory into the device table
+// `dst` (16-byte aligned) on `stream` with kernels that carry the bytes in
+// their parameters: stream-ordered, capturable in a CUDA graph, and the host
+// buffer may be reused as soon as this returns.
+cudaError_t upload_table(void *dst, const void *src, size_t bytes, cudaStream_t stream);
 int read_and_clear_gemm_pair_error();
 
 // ---------------------------------------------------------------- fused.cu

@@ -195,6 +195,14 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *tm)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }
 
+// Orders this thread's later uses of the tensor map at `tm` (in global memory,
+// written by ordinary stores of an earlier kernel) after those writes.
+__device__ __forceinline__ void tma_desc_acquire(const CUtensorMap *tm)
+{
+    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(reinterpret_cast<uint64_t>(tm))
+                 : "memory");
+}
+
 // 2-D tiled load of box {x (innermost, bytes for u8), y} into shared memory,
 // completing `bar`'s transaction count. `policy` is an L2 cache-hint policy.
 __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *tm, int32_t x,

@@ -79,6 +79,8 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.mxfp4_workspace_bytes.argtypes = [_i64, _i64, _i64]
     L.nvfp4_group_workspace_bytes.restype = _sz
     L.nvfp4_group_workspace_bytes.argtypes = [ctypes.c_int]
+    L.mxfp4_group_workspace_bytes.restype = _sz
+    L.mxfp4_group_workspace_bytes.argtypes = [ctypes.c_int]
     for name in ("mxfp4_quantize", "nvfp4_quantize"):
         f = getattr(L, name)
         f.restype = _st
@@ -113,7 +115,7 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.nvfp4_group_quant_gemm.restype = _st
     L.nvfp4_group_quant_gemm.argtypes = [ctypes.POINTER(NvActProblem), ctypes.c_int, _p, _sz, _p]
     L.mxfp4_group_gemm.restype = _st
-    L.mxfp4_group_gemm.argtypes = [ctypes.POINTER(MxProblem), ctypes.c_int, _p]
+    L.mxfp4_group_gemm.argtypes = [ctypes.POINTER(MxProblem), ctypes.c_int, _p, _sz, _p]
     L.mxfp4_group_gemm_plan.restype = _st
     L.mxfp4_group_gemm_plan.argtypes = [ctypes.POINTER(MxProblem), ctypes.c_int, ctypes.POINTER(Plan)]
     return L
@@ -331,11 +333,25 @@ def make_mx_problems(groups):
     return make_nv_problems(groups, MxProblem)
 
 
-def mxfp4_group_gemm(groups, problems=None, stream=None):
+def group_workspace(num_groups: int, device="cuda", nvfp4: bool = True):
+    """Workspace for a grouped GEMM of num_groups problems (None when none is
+    needed: up to 16 problems travel in kernel parameters)."""
+    n = int((_lib.nvfp4_group_workspace_bytes if nvfp4 else _lib.mxfp4_group_workspace_bytes)(num_groups))
+    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
+
+
+def _ws_args(workspace):
+    return (workspace.data_ptr(), workspace.numel()) if workspace is not None else (None, 0)
+
+
+def mxfp4_group_gemm(groups, problems=None, workspace=None, stream=None):
     """Grouped MXFP4 GEMM (bf16 C) over `groups` (see make_mx_problems); returns the C list."""
     if problems is None:
         problems = make_mx_problems(groups)
-    _check(_lib.mxfp4_group_gemm(problems, len(problems), _stream_ptr(stream)), "mxfp4_group_gemm")
+    if workspace is None and len(problems) > NVFP4_MAX_GROUPS:
+        workspace = group_workspace(len(problems), groups[0]["c"].device, nvfp4=False)
+    _check(_lib.mxfp4_group_gemm(problems, len(problems), *_ws_args(workspace), _stream_ptr(stream)),
+           "mxfp4_group_gemm")
     return [g["c"] for g in groups]
 
 
@@ -346,11 +362,13 @@ def mxfp4_group_gemm_plan(problems) -> dict:
     return _plan_dict(p)
 
 
-def nvfp4_group_gemm(groups, problems=None, stream=None):
+def nvfp4_group_gemm(groups, problems=None, workspace=None, stream=None):
     """Grouped NVFP4 GEMM over `groups` (see make_nv_problems); returns the C list."""
     if problems is None:
         problems = make_nv_problems(groups)
-    _check(_lib.nvfp4_group_gemm(problems, len(problems), None, 0, _stream_ptr(stream)),
+    if workspace is None and len(problems) > NVFP4_MAX_GROUPS:
+        workspace = group_workspace(len(problems), groups[0]["c"].device)
+    _check(_lib.nvfp4_group_gemm(problems, len(problems), *_ws_args(workspace), _stream_ptr(stream)),
            "nvfp4_group_gemm")
     return [g["c"] for g in groups]
 

@@ -197,20 +197,30 @@ typedef struct {
     int64_t lda, ldb, ldc;
 } nvfp4_problem_t;
 
-/* Maximum number of problems in one nvfp4_group_gemm call. */
+/* Problems a grouped call carries in its kernel parameters; a longer list
+ * (any length up to 2^20) goes through a problem table that the call writes
+ * into the caller's workspace (see nvfp4_group_workspace_bytes). */
 #define NVFP4_MAX_GROUPS 16
 
-/* Workspace bytes for nvfp4_group_gemm (currently 0: the grouped kernel keeps
- * its problem table in kernel parameters). */
+/* Workspace bytes nvfp4_group_gemm needs for num_groups problems: 0 up to
+ * NVFP4_MAX_GROUPS, else 640 bytes per problem (the device problem table:
+ * four TMA descriptors and one problem record per group). 0 for an invalid
+ * count. */
 MXFP4_API size_t nvfp4_group_workspace_bytes(int num_groups);
 
 /* Grouped NVFP4 GEMM: for each problem g,
  *   C_g[m, n] = fp16_rne( sum_k e2m1(a[m,k]) e4m3(sfa[m,k/16]) e2m1(b[n,k]) e4m3(sfb[n,k/16]) )
  * with fp32 accumulation (tcgen05.mma kind::mxf4nvf4, scale_vec::4X), all
- * groups in ONE launch scheduled tile by tile ([NV-496271] custom_kernel runs one
- * launch per group and batch index; a batch index l is flattened into extra
- * problems by the caller). `problems` is a host array of num_groups entries
- * (1 <= num_groups <= NVFP4_MAX_GROUPS); it is read during the call only. */
+ * groups in ONE GEMM launch scheduled tile by tile ([NV-496271] custom_kernel
+ * runs one launch per group and batch index; a batch index l is flattened
+ * into extra problems by the caller). `problems` is a host array of
+ * num_groups entries (1 <= num_groups <= 2^20); it is read during the call
+ * only. With more than NVFP4_MAX_GROUPS problems the call writes its problem
+ * table into `workspace` (ws_bytes >= nvfp4_group_workspace_bytes, 64-byte
+ * aligned) with small copy kernels enqueued on `stream` ahead of the GEMM, so
+ * the call stays stream-ordered and can be captured in a CUDA graph; calls
+ * that share a workspace must not overlap. Up to NVFP4_MAX_GROUPS problems the
+ * workspace is not used (may be NULL). */
 MXFP4_API mxfp4_status_t nvfp4_group_gemm(const nvfp4_problem_t *problems, int num_groups, void *workspace,
                                 size_t ws_bytes, void *stream);
 
@@ -247,18 +257,19 @@ typedef struct {
 } nvfp4_act_problem_t;
 
 /* Workspace bytes nvfp4_group_quant_gemm needs for these problems (every
- * group's quantized A and its scales), or 0 if the list is invalid. Pointers
- * are not read. */
+ * group's quantized A and its scales, then the problem table for lists longer
+ * than NVFP4_MAX_GROUPS), or 0 if the list is invalid. Pointers are not read. */
 MXFP4_API size_t nvfp4_group_quant_gemm_workspace_bytes(const nvfp4_act_problem_t *problems, int num_groups);
 
 /* Dynamic NVFP4 quantization of every group's bf16 A followed by the grouped
- * NVFP4 GEMM: one launch quantizes all A_g with nvfp4_quantize's rule and
- * layout into the workspace, a second (in stream order) computes every C_g as
- * nvfp4_group_gemm does from those operands. `problems` is a host array of
- * num_groups entries (1 <= num_groups <= NVFP4_MAX_GROUPS), read during the
- * call only. `workspace`: caller-owned device memory of at least
- * nvfp4_group_quant_gemm_workspace_bytes bytes, 16-byte aligned; it needs no
- * initialisation and afterwards holds the quantized A_g (layout not part of
+ * NVFP4 GEMM: one launch per NVFP4_MAX_GROUPS groups quantizes the A_g with
+ * nvfp4_quantize's rule and layout into the workspace, then (in stream order)
+ * one GEMM launch computes every C_g as nvfp4_group_gemm does from those
+ * operands. `problems` is a host array of num_groups entries (1 <= num_groups
+ * <= 2^20), read during the call only. `workspace`: caller-owned device
+ * memory of at least nvfp4_group_quant_gemm_workspace_bytes bytes, 16-byte
+ * aligned (64-byte aligned with more than NVFP4_MAX_GROUPS problems); it needs
+ * no initialisation and afterwards holds the quantized A_g (layout not part of
  * the ABI). Every argument is validated before anything is enqueued; a too
  * small workspace gives MXFP4_ERR_WORKSPACE_TOO_SMALL. */
 MXFP4_API mxfp4_status_t nvfp4_group_quant_gemm(const nvfp4_act_problem_t *problems, int num_groups,
@@ -278,16 +289,22 @@ typedef struct {
     int64_t lda, ldb, ldc;
 } mxfp4_problem_t;
 
-/* Maximum number of problems in one mxfp4_group_gemm call. */
+/* Problems mxfp4_group_gemm carries in its kernel parameters; longer lists
+ * go through a problem table in the workspace, as for nvfp4_group_gemm. */
 #define MXFP4_MAX_GROUPS 16
+
+/* Workspace bytes mxfp4_group_gemm needs for num_groups problems (0 up to
+ * MXFP4_MAX_GROUPS, else 640 bytes per problem). */
+MXFP4_API size_t mxfp4_group_workspace_bytes(int num_groups);
 
 /* Grouped MXFP4 GEMM: for each problem g,
  *   C_g[m, n] = bf16_rne( sum_k e2m1(a[m,k]) 2^(sfa[m,k/32]-127) e2m1(b[n,k]) 2^(sfb[n,k/32]-127) )
  * with fp32 accumulation (tcgen05.mma kind::mxf4, scale_vec::2X), all groups
- * in ONE launch scheduled tile by tile, as nvfp4_group_gemm does for NVFP4.
- * `problems` is a host array of num_groups entries (1 <= num_groups <=
- * MXFP4_MAX_GROUPS), read during the call only. Needs no workspace. */
-MXFP4_API mxfp4_status_t mxfp4_group_gemm(const mxfp4_problem_t *problems, int num_groups, void *stream);
+ * in ONE GEMM launch scheduled tile by tile, as nvfp4_group_gemm does for
+ * NVFP4, with the same rules for the problem list (1 <= num_groups <= 2^20)
+ * and the workspace (used only with more than MXFP4_MAX_GROUPS problems). */
+MXFP4_API mxfp4_status_t mxfp4_group_gemm(const mxfp4_problem_t *problems, int num_groups, void *workspace,
+                                          size_t ws_bytes, void *stream);
 
 /* Bytes of the fixed device scratch array behind mxfp4_gemm_a4w4_noalloc
  * (8 MiB). */

@@ -14,9 +14,16 @@ L = mxfp4.lib()
 
 def test_every_declared_symbol_is_exported():
     names = mxfp4.declared_symbols()
-    assert len(names) == 23
+    assert len(names) == 24
     for n in names:
         assert hasattr(L, n), n  # ctypes resolves the exported symbol
+
+
+def test_group_workspace_sizes():
+    for f in (L.nvfp4_group_workspace_bytes, L.mxfp4_group_workspace_bytes):
+        assert f(1) == 0 and f(16) == 0                      # kernel parameters carry up to 16 problems
+        assert f(17) == 17 * 640 and f(256) == 256 * 640     # 4 TMA descriptors + one record per problem
+        assert f(0) == 0 and f(-3) == 0 and f((1 << 20) + 1) == 0
 
 
 def test_wait_limit_setter_returns_previous_and_zero_restores_default():
@@ -30,7 +37,7 @@ def test_status_strings_and_version():
     for code, name in mxfp4.STATUS.items():
         assert L.mxfp4_status_string(code).decode() == name
     assert L.mxfp4_status_string(99).decode() == "MXFP4_UNKNOWN_STATUS"
-    assert L.mxfp4_abi_version() == 1
+    assert L.mxfp4_abi_version() == 2
 
 
 @pytest.mark.parametrize("rows,k,vec,want", [
@@ -95,7 +102,11 @@ def test_group_gemm_validation_needs_no_gpu():
     assert L.nvfp4_group_gemm(None, 1, None, 0, None) == 1
     assert L.nvfp4_group_gemm(arr, 0, None, 0, None) == 1
     many = (P * 17)(*([good] * 17))
-    assert L.nvfp4_group_gemm(many, 17, None, 0, None) == 2
+    # more than 16 problems: the device problem table needs a workspace
+    assert L.nvfp4_group_gemm(many, 17, None, 0, None) == 1
+    assert L.nvfp4_group_gemm(many, 17, 64, 17 * 640 - 1, None) == 4
+    assert L.nvfp4_group_gemm(many, 17, 16, 17 * 640, None) == 3     # table needs 64-byte alignment
+    assert L.nvfp4_group_gemm(many, (1 << 20) + 1, 64, 1 << 40, None) == 2
     bad_k = (P * 1)(P(64, 128, 250, 16, 16, 16, 16, 16, 128, 128, 128))
     assert L.nvfp4_group_gemm(bad_k, 1, None, 0, None) == 2
     bad_al = (P * 1)(P(64, 128, 256, 24, 16, 16, 16, 16, 128, 128, 128))
@@ -120,7 +131,7 @@ def test_plan_argument_validation_needs_no_gpu():
     probs = (mxfp4.NvProblem * 1)()
     probs[0] = mxfp4.NvProblem(64, 256, 100, 16, 16, 16, 16, 16, 64, 128, 256)
     assert L.nvfp4_group_gemm_plan(probs, 1, ctypes.byref(plan)) == 2      # K % 16
-    assert L.nvfp4_group_gemm_plan(probs, 17, ctypes.byref(plan)) == 2     # too many groups
+    assert L.nvfp4_group_gemm_plan(probs, 1, ctypes.byref(plan)) == 2      # (same list, K % 16)
 
 
 @pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="checks the no-GPU answer")
@@ -135,15 +146,17 @@ def test_mx_group_gemm_validation_needs_no_gpu():
     good[0] = P(64, 256, 512, 16, 16, 16, 16, 16, 256, 256, 256)
     bad_k = (P * 1)()
     bad_k[0] = P(64, 256, 48, 16, 16, 16, 16, 16, 32, 32, 256)      # K % 32
-    assert L.mxfp4_group_gemm(bad_k, 1, None) == 2
+    assert L.mxfp4_group_gemm(bad_k, 1, None, 0, None) == 2
     null = (P * 1)()
     null[0] = P(64, 256, 512, 0, 16, 16, 16, 16, 256, 256, 256)     # null A
-    assert L.mxfp4_group_gemm(null, 1, None) == 1
+    assert L.mxfp4_group_gemm(null, 1, None, 0, None) == 1
     bad_al = (P * 1)()
     bad_al[0] = P(64, 256, 512, 16, 16, 16, 16, 16, 264, 256, 256)  # lda % 16
-    assert L.mxfp4_group_gemm(bad_al, 1, None) == 3
-    assert L.mxfp4_group_gemm(good, 17, None) == 2                   # too many groups
-    assert L.mxfp4_group_gemm(None, 1, None) == 1
+    assert L.mxfp4_group_gemm(bad_al, 1, None, 0, None) == 3
+    many = (P * 20)(*([good[0]] * 20))
+    assert L.mxfp4_group_gemm(many, 20, None, 0, None) == 1          # more than 16 need a workspace
+    assert L.mxfp4_group_gemm(many, 20, 64, 20 * 640 - 64, None) == 4
+    assert L.mxfp4_group_gemm(None, 1, None, 0, None) == 1
     plan = mxfp4.Plan()
     assert L.mxfp4_group_gemm_plan(bad_k, 1, ctypes.byref(plan)) == 2
 
@@ -197,7 +210,10 @@ def test_group_quant_gemm_validation_needs_no_gpu():
     assert f(one(), 1, None, big, None) == 1               # no workspace
     assert f(one(), 1, 24, big, None) == 3                 # workspace alignment
     assert f(one(), 1, 16, 64 * 256, None) == 4            # workspace too small
-    assert f(one(), 17, 16, big, None) == 2                # too many groups
+    seventeen = (P * 17)(*([one()[0]] * 17))
+    per = 64 * 256 + 128 * 32
+    assert ws_fn(seventeen, 17) == 17 * per + 17 * 640      # + the device problem table
+    assert f(seventeen, 17, 64, 17 * per + 17 * 640 - 1, None) == 4
     assert f(None, 1, 16, big, None) == 1
 
 

@@ -75,3 +75,14 @@ def test_matches_the_single_problem_gemm():
     torch.cuda.synchronize()
     d = (c.float() - ref.float()).abs()
     assert float(d.max()) <= 2.0 ** -7 * float(ref.float().abs().max()) + 1e-3
+
+
+def test_forty_groups_device_table():
+    """More than 16 MXFP4 problems through the device problem table."""
+    shapes = [(2 + 11 * i, 64 + 64 * (i % 4), 64 + 32 * (i % 5)) for i in range(40)]
+    run_groups(shapes, 9, "bs_gemm_kernel")
+
+
+def test_groups_on_cta_pairs_device_table():
+    shapes = [(256 + 5 * (i % 4), 1024, 128 + 64 * (i % 2)) for i in range(20)]
+    run_groups(shapes, 10, "bs_gemm_pair_kernel")

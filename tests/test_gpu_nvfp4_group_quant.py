@@ -74,3 +74,9 @@ def test_ragged_groups_cta_pairs_strided_a():
 
 def test_sixteen_groups():
     run([(8 + 40 * i, 128 + 64 * (i % 3), 64 + 48 * (i % 4)) for i in range(16)], 4)
+
+
+def test_thirty_five_groups():
+    """More than 16 groups: the quantization runs in launches of 16 groups and
+    the GEMM reads its problems from the table after the quantized A_g."""
+    run([(3 + 17 * i, 64 + 64 * (i % 4), 64 + 32 * (i % 5)) for i in range(35)], 5)
