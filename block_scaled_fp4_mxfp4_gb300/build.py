@@ -37,7 +37,7 @@ def _sources():
 
 def _deps():
     return _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h"))
-                               + glob.glob(os.path.join(INCLUDE, "*.h")))
+                               + glob.glob(os.path.join(CSRC, "*.inc")) + glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
 def up_to_date() -> bool:

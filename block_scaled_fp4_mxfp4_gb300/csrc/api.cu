@@ -221,6 +221,31 @@ size_t sf_bytes(int64_t rows, int64_t k, int vec)
     return static_cast<size_t>((rows + 127) / 128) * static_cast<size_t>((k / vec + 3) / 4) * 512;
 }
 
+// ------------------------------------------------------- split-K choices
+#include "split_table.inc"
+
+// Process-wide tuning override of the K-splits (0: none), per path: 0 the
+// two-kernel GEMM, 1 the fused MXFP4 kernel, 2 the fused NVFP4 kernel.
+std::atomic<int> g_split_override[3] = {};
+
+int split_bucket(int which, int64_t M)
+{
+    if (which == 0) return static_cast<int>((M + 127) / 128);
+    return M <= 16 ? 16 : M <= 32 ? 32 : 64;
+}
+
+// K-splits asked for (M, N, K) on a path: the override, else the measured
+// table's entry, else 0 (the shape-derived rule decides).
+int split_choice(int which, int64_t M, int64_t N, int64_t K)
+{
+    const int o = g_split_override[which].load(std::memory_order_relaxed);
+    if (o > 0) return o;
+    const int b = split_bucket(which, M);
+    for (const SplitEntry *e = kSplitTable; e->which >= 0; ++e)
+        if (e->which == which && e->bucket == b && e->n == N && e->k == K) return e->splits;
+    return 0;
+}
+
 struct GemmPlan {
     bool pair;     // CTA-pair kernel (256 x 256 tiles); else single-CTA 128 x bn tiles
     int bn;        // single-CTA tile width along N: 256, or 128 when 256-wide tiles leave
@@ -258,6 +283,13 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K)
         if (s > kMaxSplitK) s = kMaxSplitK;
         // keep the fp32 partial traffic well below the weight bytes
         while (s > 1 && s * M * N * 4 > N * (K / 2) / 2) --s;
+        if (s < 1) s = 1;
+    }
+    const int want = split_choice(0, M, N, K);
+    if (want > 0) {
+        s = want;
+        if (s > kMaxSplitK) s = kMaxSplitK;
+        if (s > k_stages) s = k_stages;
         if (s < 1) s = 1;
     }
     p.splits = static_cast<int>(s);
@@ -613,7 +645,7 @@ mxfp4_status_t mxfp4_quant_gemm_fused(const void *A, int64_t lda, const void *Bq
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     FusedPlan fp;
-    if (plan_fused(M, N, K, sms, &fp)) {
+    if (plan_fused(M, N, K, sms, &fp, false, split_choice(1, M, N, K))) {
         CUtensorMap tmw;
         st = fp4_map(Bq, K / 2, N, ldbq, 128, &tmw);
         if (st != MXFP4_OK) return st;
@@ -642,7 +674,7 @@ mxfp4_status_t nvfp4_quant_gemm_fused(const void *A, int64_t lda, const void *Bq
     mxfp4_status_t st = current_device(&sms);
     if (st != MXFP4_OK) return st;
     FusedPlan fp;
-    if (!plan_fused(M, N, K, sms, &fp, true)) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+    if (!plan_fused(M, N, K, sms, &fp, true, split_choice(2, M, N, K))) return MXFP4_ERR_UNSUPPORTED_SHAPE;
     CUtensorMap tmw;
     st = fp4_map(Bq, K / 2, N, ldbq, 128, &tmw);
     if (st != MXFP4_OK) return st;
@@ -738,7 +770,7 @@ mxfp4_status_t mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, int which, mxfp4
     if (st != MXFP4_OK) return st;
     memset(out, 0, sizeof(*out));
     FusedPlan fp;
-    if (which >= 1 && plan_fused(M, N, K, sms, &fp, which == 2)) {
+    if (which >= 1 && plan_fused(M, N, K, sms, &fp, which == 2, split_choice(which, M, N, K))) {
         out->kernel = MXFP4_KERNEL_FUSED;
         out->tile_m = fp.mma_n;   // activation rows (padded) x 128 weight rows
         out->tile_n = 128;
@@ -765,6 +797,26 @@ mxfp4_status_t nvfp4_group_gemm_plan(const nvfp4_problem_t *problems, int num_gr
 mxfp4_status_t mxfp4_group_gemm_plan(const mxfp4_problem_t *problems, int num_groups, mxfp4_plan_t *out)
 {
     return group_gemm_plan(problems, num_groups, false, out);
+}
+
+int mxfp4_set_split_override(int path, int splits)
+{
+    if (path < 0 || path > 2 || splits < 0) return -1;
+    return g_split_override[path].exchange(splits);
+}
+
+int mxfp4_split_table_entry(int index, int *path, int *bucket, int64_t *n, int64_t *k, int *splits)
+{
+    int count = 0;
+    while (kSplitTable[count].which >= 0) ++count;
+    if (index < 0 || index >= count) return count;
+    const SplitEntry &e = kSplitTable[index];
+    if (path) *path = e.which;
+    if (bucket) *bucket = e.bucket;
+    if (n) *n = e.n;
+    if (k) *k = e.k;
+    if (splits) *splits = e.splits;
+    return count;
 }
 
 uint64_t mxfp4_set_wait_limit_ns(uint64_t ns)

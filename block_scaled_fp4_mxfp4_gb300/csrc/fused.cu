@@ -33,6 +33,7 @@
 //   deterministic.
 // Shared memory stays near 100 KB (MMA_N = 16) so two CTAs fit on an SM and
 // every cluster of the grid can be resident at once.
+#include <algorithm>
 #include <cstring>
 
 #include "internal.h"
@@ -466,7 +467,7 @@ cudaError_t launch_fused_t(const CUtensorMap &tmw, const FusedArgs &args, int n_
 
 }  // namespace
 
-bool plan_fused(int64_t M, int64_t N, int64_t K, int num_sms, FusedPlan *plan, bool nvfp4)
+bool plan_fused(int64_t M, int64_t N, int64_t K, int num_sms, FusedPlan *plan, bool nvfp4, int want_splits)
 {
     if (M < 1 || M > 64 || N < 1 || K < (nvfp4 ? 16 : 32)) return false;
     const int mma_n = M <= 16 ? 16 : M <= 32 ? 32 : 64;
@@ -481,6 +482,7 @@ bool plan_fused(int64_t M, int64_t N, int64_t K, int num_sms, FusedPlan *plan, b
     if (s < 1) s = 1;
     if (s > k_stages) s = k_stages;
     const int64_t s_min = (k_stages + max_st - 1) / max_st;
+    if (want_splits > 0) s = std::min<int64_t>(std::min<int64_t>(want_splits, kMaxSplits), k_stages);
     if (s < s_min) s = s_min;
     if (s > kMaxSplits || n_tiles > 0x7fffffff) return false;
     plan->mma_n = mma_n;

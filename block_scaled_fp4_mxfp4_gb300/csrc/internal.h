@@ -155,7 +155,20 @@ struct FusedPlan {
 };
 // Whether the fused small-M kernel can run (M, K) and with which plan.
 // nvfp4: E4M3 scales per 16 and fp16 C (else MXFP4: E8M0 per 32, bf16 C).
-bool plan_fused(int64_t M, int64_t N, int64_t K, int num_sms, FusedPlan *plan, bool nvfp4 = false);
+// want_splits > 0 asks for that many K-splits (clamped to what the kernel
+// can run); 0 takes the shape-derived rule.
+bool plan_fused(int64_t M, int64_t N, int64_t K, int num_sms, FusedPlan *plan, bool nvfp4 = false,
+                int want_splits = 0);
+
+// One entry of the measured split-K table (csrc/split_table.inc): the
+// K-splits that were fastest for a shape. which: 0 = two-kernel GEMM path
+// (bucket = 128-row tiles of M), 1 = fused MXFP4, 2 = fused NVFP4 (bucket =
+// MMA width 16 / 32 / 64 of the padded activation rows).
+struct SplitEntry {
+    int which, bucket;
+    int64_t n, k;
+    int splits;
+};
 // tmb: packed weights [N, K/2], box {128 B, 128 rows}, 128B swizzle.
 cudaError_t launch_fused(const CUtensorMap &tmb, const void *A, int64_t lda, const uint8_t *sfb,
                          void *C, int64_t ldc, int M, int N, int K, const FusedPlan &plan, bool nvfp4,

@@ -104,6 +104,10 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.mxfp4_gemm_a4w4_noalloc.argtypes = [_p, _i64, _p, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p]
     L.mxfp4_get_device_error.restype = _st
     L.mxfp4_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    L.mxfp4_set_split_override.restype = ctypes.c_int
+    L.mxfp4_set_split_override.argtypes = [ctypes.c_int, ctypes.c_int]
+    L.mxfp4_split_table_entry.restype = ctypes.c_int
+    L.mxfp4_split_table_entry.argtypes = [ctypes.c_int] + [ctypes.c_void_p] * 5
     L.mxfp4_set_wait_limit_ns.restype = ctypes.c_uint64
     L.mxfp4_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     L.mxfp4_gemm_plan.restype = _st
@@ -424,6 +428,33 @@ def nvfp4_group_gemm_plan(problems) -> dict:
     p = Plan()
     _check(lib().nvfp4_group_gemm_plan(problems, len(problems), ctypes.byref(p)), "nvfp4_group_gemm_plan")
     return _plan_dict(p)
+
+
+SPLIT_PATHS = {"gemm": 0, "fused": 1, "fused_nv": 2}
+
+
+def set_split_override(path: str, splits: int) -> int:
+    """Override the K-splits of later calls on `path` ("gemm", "fused",
+    "fused_nv"; 0 clears); returns the previous override."""
+    r = int(_lib.mxfp4_set_split_override(SPLIT_PATHS[path], int(splits)))
+    if r < 0:
+        raise ValueError("bad split override")
+    return r
+
+
+def split_table():
+    """The measured split-K table built into the library: a list of dicts
+    (path, bucket, n, k, splits)."""
+    names = {v: k for k, v in SPLIT_PATHS.items()}
+    n = int(_lib.mxfp4_split_table_entry(-1, None, None, None, None, None))
+    out = []
+    for i in range(n):
+        path, bucket, splits = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+        nn, kk = ctypes.c_int64(), ctypes.c_int64()
+        _lib.mxfp4_split_table_entry(i, ctypes.byref(path), ctypes.byref(bucket), ctypes.byref(nn),
+                                     ctypes.byref(kk), ctypes.byref(splits))
+        out.append(dict(path=names[path.value], bucket=bucket.value, n=nn.value, k=kk.value, splits=splits.value))
+    return out
 
 
 def set_wait_limit_ns(ns: int) -> int:

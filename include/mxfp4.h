@@ -382,6 +382,27 @@ MXFP4_API mxfp4_status_t mxfp4_group_gemm_plan(const mxfp4_problem_t *problems, 
  * (CTA-pair GEMM), c naming the wait that gave up. */
 MXFP4_API mxfp4_status_t mxfp4_get_device_error(int *code);
 
+/* K-splits of the split-K paths. The planner takes, in this order: a tuning
+ * override set here, the entry of the measured table built into the library
+ * for the shape (exact N and K; M by bucket), or its shape-derived rule. The
+ * plan functions above report the result. */
+#define MXFP4_SPLITS_GEMM 0        /* two-kernel path: bucket = 128-row tiles of M */
+#define MXFP4_SPLITS_FUSED 1       /* fused MXFP4 kernel: bucket = MMA width 16/32/64 */
+#define MXFP4_SPLITS_FUSED_NV 2    /* fused NVFP4 kernel: bucket = MMA width 16/32/64 */
+
+/* Sets (splits > 0) or clears (0) a process-wide override of the K-splits of
+ * every later call on `path`, clamped per call to what the kernel can run;
+ * returns the previous override, or -1 for a bad argument. Meant for tuning
+ * (the table is written by block_scaled_fp4_mxfp4_gb300/tune_splits.py): the
+ * workspace a shape needs follows the override, so query
+ * mxfp4_workspace_bytes after setting it. */
+MXFP4_API int mxfp4_set_split_override(int path, int splits);
+
+/* Entry `index` of the measured split-K table (any pointer may be NULL);
+ * returns the number of entries (and fills nothing when index is out of
+ * range). */
+MXFP4_API int mxfp4_split_table_entry(int index, int *path, int *bucket, int64_t *n, int64_t *k, int *splits);
+
 /* Sets the time limit, in nanoseconds, of the waits that guard work inside
  * every kernel launched afterwards (process-wide; 0 restores the default of
  * 2 s) and returns the previous limit. The waits on a kernel's exit path,

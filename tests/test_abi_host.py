@@ -14,7 +14,7 @@ L = mxfp4.lib()
 
 def test_every_declared_symbol_is_exported():
     names = mxfp4.declared_symbols()
-    assert len(names) == 24
+    assert len(names) == 26
     for n in names:
         assert hasattr(L, n), n  # ctypes resolves the exported symbol
 

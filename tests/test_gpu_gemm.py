@@ -33,7 +33,7 @@ def inputs(M, N, K, seed, a_scale=1.0, b_scale=1.0):
 
 GEMM_SHAPES = [
     (1, 1, 32), (8, 512, 1024), (128, 256, 256), (130, 300, 96), (256, 512, 512),
-    (200, 384, 2080), (16, 512, 4096), (64, 1000, 1536), (300, 130, 64), (129, 257, 288),
+    (200, 384, 2080), (16, 512, 4096), (16, 640, 4096), (64, 1000, 1536), (300, 130, 64), (129, 257, 288),
     # enough tiles for 256-wide tiles: ragged second half-tile, a partial last K stage
     (1300, 1900, 320),
     # at least one 256 x 256 tile per SM pair: the CTA-pair kernel. 80 tiles (some

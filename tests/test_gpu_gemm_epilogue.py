@@ -16,7 +16,7 @@ mx = pytest.importorskip("block_scaled_fp4_mxfp4_gb300.mxfp4")
 
 SHAPES = [
     ((130, 300, 96), "bs_gemm_kernel", 1),          # 128-wide tiles, ragged
-    ((16, 512, 4096), "bs_gemm_kernel", 2),         # split-K: epilogue in the final reduction
+    ((16, 640, 4096), "bs_gemm_kernel", 2),         # split-K: epilogue in the final reduction
     ((1300, 1900, 320), "bs_gemm_kernel", 1),       # 256-wide tiles
     ((2100, 2100, 96), "bs_gemm_pair_kernel", 1),   # CTA pairs, ragged
 ]

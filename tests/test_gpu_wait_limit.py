@@ -27,7 +27,7 @@ mx = pytest.importorskip("block_scaled_fp4_mxfp4_gb300.mxfp4")
 # within one tick of that timer).
 CASES = {
     "gemm": ("gemm", 256, 512, 2048, "bs_gemm_kernel", (1, 15)),
-    "gemm_splitk": ("gemm", 16, 512, 4096, "bs_gemm_kernel", (1, 15)),
+    "gemm_splitk": ("gemm", 16, 640, 4096, "bs_gemm_kernel", (1, 15)),
     "fused_mxfp4": ("fused", 16, 8192, 7168, "fused_quant_gemm_kernel", (17, 31)),
     "fused_nvfp4": ("fused_nv", 16, 8192, 7168, "fused_quant_gemm_kernel", (17, 31)),
     "pair": ("gemm", 2560, 2048, 512, "bs_gemm_pair_kernel", (33, 47)),
