@@ -689,19 +689,26 @@ mxfp4_status_t nvfp4_group_gemm(const nvfp4_problem_t *problems, int num_groups,
     return group_gemm(problems, num_groups, true, workspace, ws_bytes, stream);
 }
 
-mxfp4_status_t mxfp4_rmsnorm_quantize(const void *X, int64_t M, int64_t K, int64_t ldx, const void *weight,
-                                      float eps, void *Aq, int64_t ldq, void *A_sf, void *stream)
+mxfp4_status_t mxfp4_rmsnorm_quantize_ex(const void *X, int64_t M, int64_t K, int64_t ldx, const void *weight,
+                                         float eps, void *Aq, int64_t ldq, void *A_sf, float *rstd, double *sumsq,
+                                         void *stream)
 {
     mxfp4_status_t st = check_quant(X, M, K, ldx, Aq, ldq, A_sf, 32);
     if (st != MXFP4_OK) return st;
     if (!weight) return MXFP4_ERR_INVALID_ARG;
     if (!(eps >= 0.0f) || !std::isfinite(eps)) return MXFP4_ERR_INVALID_ARG;
-    if (!al16(weight)) return MXFP4_ERR_MISALIGNED;
+    if (!al16(weight) || !al4(rstd) || (reinterpret_cast<uintptr_t>(sumsq) & 7u) != 0) return MXFP4_ERR_MISALIGNED;
     int sms = 0;
     st = current_device(&sms);
     if (st != MXFP4_OK) return st;
-    return cuda_status(launch_rmsnorm_mx_quant(X, M, K, ldx, weight, eps, Aq, ldq, A_sf, sms,
+    return cuda_status(launch_rmsnorm_mx_quant(X, M, K, ldx, weight, eps, Aq, ldq, A_sf, rstd, sumsq, sms,
                                                static_cast<cudaStream_t>(stream)));
+}
+
+mxfp4_status_t mxfp4_rmsnorm_quantize(const void *X, int64_t M, int64_t K, int64_t ldx, const void *weight,
+                                      float eps, void *Aq, int64_t ldq, void *A_sf, void *stream)
+{
+    return mxfp4_rmsnorm_quantize_ex(X, M, K, ldx, weight, eps, Aq, ldq, A_sf, nullptr, nullptr, stream);
 }
 
 size_t nvfp4_group_quant_gemm_workspace_bytes(const nvfp4_act_problem_t *problems, int num_groups)

@@ -83,7 +83,8 @@ cudaError_t launch_quant_nv_grouped(const QuantGroupHost *groups, int count, int
 // --------------------------------------------------------- rmsnorm_quant.cu
 // Fused RMSNorm (bf16 weight [K], eps) + MXFP4 quantization of bf16 X [M, K].
 cudaError_t launch_rmsnorm_mx_quant(const void *X, int64_t M, int64_t K, int64_t ldx, const void *w, float eps,
-                                    void *Aq, int64_t ldq, void *sf, int num_sms, cudaStream_t stream);
+                                    void *Aq, int64_t ldq, void *sf, float *rstd, double *sumsq, int num_sms,
+                                    cudaStream_t stream);
 
 // ----------------------------------------------------------------- gemm.cu
 // One GEMM problem as the tile scheduler sees it.

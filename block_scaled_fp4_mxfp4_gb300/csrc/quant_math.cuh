@@ -41,6 +41,14 @@ __device__ __forceinline__ uint32_t umax16x2(uint32_t a, uint32_t b)
     return d;
 }
 
+// Lane-wise unsigned 16-bit min of two packed pairs.
+__device__ __forceinline__ uint32_t umin16x2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 // Packed (two-lane) maximum bf16 magnitude of 8 values; bf16 magnitudes
 // compare like unsigned integers once the sign bit is cleared.
 __device__ __forceinline__ uint32_t max_abs_pair8(const uint4 &v)

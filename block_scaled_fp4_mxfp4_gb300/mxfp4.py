@@ -87,6 +87,8 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
         f.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p, _p]
     L.mxfp4_rmsnorm_quantize.restype = _st
     L.mxfp4_rmsnorm_quantize.argtypes = [_p, _i64, _i64, _i64, _p, ctypes.c_float, _p, _i64, _p, _p]
+    L.mxfp4_rmsnorm_quantize_ex.restype = _st
+    L.mxfp4_rmsnorm_quantize_ex.argtypes = [_p, _i64, _i64, _i64, _p, ctypes.c_float, _p, _i64, _p, _p, _p, _p]
     L.mxfp4_gemm_a4w4.restype = _st
     L.mxfp4_gemm_a4w4.argtypes = [_p, _i64, _p, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p, _sz, _p]
     L.mxfp4_gemm_a4w4_ex.restype = _st
@@ -205,9 +207,11 @@ def nvfp4_quantize(A, Aq=None, A_sf=None, stream=None):
     return _quant(_lib.nvfp4_quantize, 16, A, Aq, A_sf, stream, "nvfp4_quantize")
 
 
-def mxfp4_rmsnorm_quantize(X, weight, eps: float = 1e-6, Aq=None, A_sf=None, stream=None):
+def mxfp4_rmsnorm_quantize(X, weight, eps: float = 1e-6, Aq=None, A_sf=None, stream=None, stats: bool = False):
     """Fused RMSNorm + MXFP4 quantization: bf16 X [M, K], bf16 weight [K] ->
-    (packed E2M1 [M, K/2] u8, blocked E8M0 scales) of the normalized rows."""
+    (packed E2M1 [M, K/2] u8, blocked E8M0 scales) of the normalized rows.
+    With stats=True also returns each row's fp32 reciprocal r [M] and its
+    exactly rounded fp64 sum of squares [M]."""
     _dev(X, "X", torch.bfloat16, 2)
     _dev(weight, "weight", torch.bfloat16, 1)
     M, K = X.shape
@@ -220,10 +224,18 @@ def mxfp4_rmsnorm_quantize(X, weight, eps: float = 1e-6, Aq=None, A_sf=None, str
         A_sf = torch.empty(max(1, sf_bytes(M, K, 32)), dtype=torch.uint8, device=X.device)
     _dev(Aq, "Aq", torch.uint8, 2)
     _dev(A_sf, "A_sf", torch.uint8)
-    _check(_lib.mxfp4_rmsnorm_quantize(X.data_ptr(), M, K, X.stride(0), weight.data_ptr(), float(eps),
-                                       Aq.data_ptr(), Aq.stride(0), A_sf.data_ptr(), _stream_ptr(stream)),
-           "mxfp4_rmsnorm_quantize")
-    return Aq, A_sf
+    if not stats:
+        _check(_lib.mxfp4_rmsnorm_quantize(X.data_ptr(), M, K, X.stride(0), weight.data_ptr(), float(eps),
+                                           Aq.data_ptr(), Aq.stride(0), A_sf.data_ptr(), _stream_ptr(stream)),
+               "mxfp4_rmsnorm_quantize")
+        return Aq, A_sf
+    rstd = torch.empty(M, dtype=torch.float32, device=X.device)
+    sumsq = torch.empty(M, dtype=torch.float64, device=X.device)
+    _check(_lib.mxfp4_rmsnorm_quantize_ex(X.data_ptr(), M, K, X.stride(0), weight.data_ptr(), float(eps),
+                                          Aq.data_ptr(), Aq.stride(0), A_sf.data_ptr(), rstd.data_ptr(),
+                                          sumsq.data_ptr(), _stream_ptr(stream)),
+           "mxfp4_rmsnorm_quantize_ex")
+    return Aq, A_sf, rstd, sumsq
 
 
 # ------------------------------------------------------------------ GEMM --

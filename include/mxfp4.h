@@ -228,21 +228,31 @@ MXFP4_API mxfp4_status_t nvfp4_group_gemm(const nvfp4_problem_t *problems, int n
  * elements) with a bf16 weight [K] and eps: the activation step that
  * [MM-683203] ("hot path") fuses ahead of the GEMM, which the pages name
  * without giving its arithmetic. The reading this library takes, per row:
- *   ss  = sum_k x_k^2, exact, rounded once to fp64
+ *   ss  = sum_k x_k^2, exact, rounded once to fp64 (round to nearest even)
  *   r   = fp32(1 / sqrt(ss / K + eps)) computed in fp64 (r = 0 when
  *         ss / K + eps == 0)
  *   y_k = fp32(fp32(x_k * r) * weight_k)
  * and y is quantized exactly as mxfp4_quantize quantizes its input (OCP MX
  * rule per 32 values, E2M1 codes [M, K/2] with row stride ldq bytes, E8M0
  * scales in the blocked layout, mxfp4_sf_bytes(M, K, 32) bytes, pad 0x7F), so
- * the outputs feed mxfp4_gemm_a4w4 directly. The sum is exact whenever every
- * nonzero |x| of a row lies within 2^40 of the row's largest. Requirements:
- * K % 32 == 0; eps finite and >= 0; X and weight finite with every |y| finite;
- * X and weight 16-byte aligned, ldx * 2 a multiple of 16; Aq and A_sf 4-byte
+ * the outputs feed mxfp4_gemm_a4w4 directly. The sum is exact for every
+ * finite row, whatever the range of its magnitudes. Requirements: K % 32 == 0;
+ * eps finite and >= 0; X and weight finite with every |y| finite; X and
+ * weight 16-byte aligned, ldx * 2 a multiple of 16; Aq and A_sf 4-byte
  * aligned, ldq a multiple of 4. */
 MXFP4_API mxfp4_status_t mxfp4_rmsnorm_quantize(const void *X, int64_t M, int64_t K, int64_t ldx,
                                                 const void *weight, float eps, void *Aq, int64_t ldq,
                                                 void *A_sf, void *stream);
+
+/* mxfp4_rmsnorm_quantize that also stores, per row m, rstd[m] = r (the fp32
+ * reciprocal the row was scaled by, as a backward pass keeps it) and
+ * sumsq[m] = ss (the exactly rounded fp64 sum of squares). Either pointer may
+ * be NULL (not stored); otherwise device memory of M entries, rstd 4-byte and
+ * sumsq 8-byte aligned (MXFP4_ERR_MISALIGNED). Same outputs, rules and errors
+ * as mxfp4_rmsnorm_quantize otherwise. */
+MXFP4_API mxfp4_status_t mxfp4_rmsnorm_quantize_ex(const void *X, int64_t M, int64_t K, int64_t ldx,
+                                                   const void *weight, float eps, void *Aq, int64_t ldq,
+                                                   void *A_sf, float *rstd, double *sumsq, void *stream);
 
 /* One problem of a grouped NVFP4 GEMM whose activation is still bf16: the
  * [NV-496271] problem list (custom_kernel) with A given unquantized, as a

@@ -14,7 +14,7 @@ L = mxfp4.lib()
 
 def test_every_declared_symbol_is_exported():
     names = mxfp4.declared_symbols()
-    assert len(names) == 26
+    assert len(names) == 27
     for n in names:
         assert hasattr(L, n), n  # ctypes resolves the exported symbol
 
@@ -231,3 +231,11 @@ def test_rmsnorm_quantize_validation_needs_no_gpu():
     assert call(w=24) == 3                      # weight alignment
     assert call(ldx=68) == 3                    # ldx * 2 % 16
     assert call(X=None) == 1
+    g = L.mxfp4_rmsnorm_quantize_ex
+    def call_ex(rstd, sumsq, **kw):
+        a = dict(ok, **kw)
+        return g(a["X"], a["M"], a["K"], a["ldx"], a["w"], a["eps"], a["Aq"], a["ldq"], a["sf"], rstd, sumsq, None)
+    assert call_ex(None, None, K=48, ldx=48, ldq=24) == 2
+    assert call_ex(18, None) == 3               # rstd 4-byte alignment
+    assert call_ex(None, 20) == 3               # sumsq 8-byte alignment
+    assert call_ex(None, None, w=None) == 1

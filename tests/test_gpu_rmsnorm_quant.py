@@ -2,6 +2,8 @@
 oracle's reading of it: codes and E8M0 scale bytes bit-exact on ragged shapes,
 strided rows, several eps values, zero rows and rows whose norm is a power of
 two; the output also feeds the MXFP4 GEMM like mxfp4_quantize's does."""
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -66,3 +68,115 @@ def test_feeds_the_gemm():
     c_ref, s = oracle.gemm_full(qa_r, sfa_r, qb_r, sfb_r, K, 32)
     assert_within_tolerance(c_f64(C), c_ref, s, "rmsnorm-quantized GEMM")
     assert mx.get_device_error() == 0
+
+
+# ------------------------------------------------------- exact sum of squares
+def bf16_row(values, K):
+    """Row of K bf16 values (the given ones first, then zeros); every value
+    must be exactly representable in bf16."""
+    row = np.zeros(K)
+    row[:len(values)] = values
+    bits = wl.to_bf16_bits(row[None, :])[0]
+    assert np.array_equal(oracle._bf16_bits_to_f64(bits), row), "value not representable in bf16"
+    return bits
+
+
+def exact_sumsq(bits):
+    x = oracle._bf16_bits_to_f64(bits)
+    return math.fsum((x * x).tolist())   # each square is exact in fp64; fsum rounds the exact total once
+
+
+def check_stats(X_bits, w_bits, eps, what):
+    X = dev_bf16(X_bits)
+    w = dev_bf16(w_bits[None, :])[0].contiguous()
+    q, sf, rstd, ss = mx.mxfp4_rmsnorm_quantize(X, w, eps, stats=True)
+    torch.cuda.synchronize()
+    M, K = X_bits.shape
+    ss_ref = np.array([exact_sumsq(X_bits[m]) for m in range(M)])
+    got = host(ss)
+    bad = np.flatnonzero(got.view(np.int64) != ss_ref.view(np.int64))
+    assert bad.size == 0, f"{what}: rows {bad[:5]} sum of squares {got[bad[:5]]!r} != {ss_ref[bad[:5]]!r}"
+    e = float(np.float32(eps))
+    r_ref = np.array([np.float32(0.0 if s / K + e == 0.0 else 1.0 / math.sqrt(s / K + e)) for s in ss_ref],
+                     dtype=np.float32)
+    assert np.array_equal(host(rstd).view(np.int32), r_ref.view(np.int32)), f"{what}: rstd"
+    q_ref, sf_ref = oracle.rmsnorm_mx_quantize(X_bits, w_bits, eps)
+    assert_bytes_equal(host(q), q_ref, f"codes {what}")
+    assert_bytes_equal(host(sf)[:sf_ref.size], sf_ref, f"scales {what}")
+    return got
+
+
+def tie_rows():
+    """Rows whose squares at most 2^80 below the largest square sum to an exact
+    fp64 tie (or just below one), and whose squares further below decide the
+    rounding. Returns (values, what the retained squares alone round to)."""
+    rows = []
+    # 1 + 2^-54 + 2^-54 is the midpoint of 1 and 1 + 2^-52; one square of
+    # 2^-122 (|x| = 2^-61, 2^61 below the largest) breaks the tie upwards
+    rows.append([1.0, 2.0 ** -27, 2.0 ** -27, 2.0 ** -61])
+    # the same tie alone rounds to even (1.0)
+    rows.append([1.0, 2.0 ** -27, 2.0 ** -27])
+    # 2^40 + (2^-13 - 2^-40) lies 2^-40 below the midpoint of 2^40 and
+    # 2^40 + 2^-12; 256 squares of 2^-42 (2^41 below the largest |x|) add 2^-34,
+    # more than one unit of a 2^-80-relative window, and carry it over
+    vals = [2.0 ** 20]
+    for i in range(14, 41):
+        vals += [2.0 ** (-i / 2)] if i % 2 == 0 else [2.0 ** (-(i + 1) / 2)] * 2
+    rows.append(vals + [2.0 ** -21] * 256)
+    rows.append(vals)                      # without them: rounds down
+    # the largest bf16 exponent with subnormal squares below it (a 2^260 span)
+    rows.append([1.5 * 2.0 ** 127, -(2.0 ** -133), 3 * 2.0 ** -133, 2.0 ** 100, -(2.0 ** -60)])
+    return rows
+
+
+def test_sum_of_squares_is_exact_across_any_range():
+    K = 384
+    rows = tie_rows()
+    X = np.stack([bf16_row(v, K) for v in rows])
+    # pins on the construction: the squares far below decide the rounding
+    s = [exact_sumsq(X[i]) for i in range(len(rows))]
+    assert s[0] == 1.0 + 2.0 ** -52 and s[1] == 1.0
+    assert s[2] == 2.0 ** 40 + 2.0 ** -12 and s[3] == 2.0 ** 40
+    w = wl.gen_bf16(15, 2, 1, K)[0]
+    for eps in (0.0, 1e-6):
+        check_stats(X, w, eps, f"tie rows eps={eps}")
+
+
+def test_sum_of_squares_exponent_boundaries():
+    """Values at exactly 16, 17, 40 and 41 binades below the largest (the
+    limits of the 64-bit, 128-bit and limb paths), all-subnormal rows and rows
+    whose largest value is tiny (every square takes the 128-bit path)."""
+    K = 64
+    rows = []
+    for top in (0.0, -60.0, 90.0, 127.0):
+        big = 2.0 ** top * 1.75
+        rows.append([big] + [1.5 * 2.0 ** (top - d) for d in (15, 16, 17, 39, 40, 41, 42)])
+    rows.append([3 * 2.0 ** -133, 2.0 ** -133, 127 * 2.0 ** -133])          # subnormals only
+    rows.append([2.0 ** -110, 2.0 ** -111, 2.0 ** -126, 5 * 2.0 ** -133])   # largest field 17 / 16
+    rows.append([2.0 ** -112, 2.0 ** -120, 2.0 ** -133])
+    rows.append([])                                                         # zeros
+    X = np.stack([bf16_row(v, K) for v in rows])
+    check_stats(X, wl.gen_bf16(16, 2, 1, K)[0], 1e-6, "boundaries")
+    # with eps = 0 the all-subnormal row has r = 2^129, beyond fp32 (outside
+    # the documented domain: every |y| finite); the others keep a finite r
+    keep = [i for i in range(len(rows)) if i != 4]
+    assert exact_sumsq(X[4]) / K < 2.0 ** -256
+    check_stats(X[keep], wl.gen_bf16(16, 2, 1, K)[0], 0.0, "boundaries eps=0")
+
+
+def test_sum_of_squares_random_wide_rows():
+    """Random rows whose magnitudes span up to 2^200 (every path, shared
+    atomics from many threads), several row lengths including chunked rows."""
+    rng = np.random.default_rng(17)
+    for M, K in ((9, 7168), (4, 2048), (3, 139264)):
+        e = rng.integers(-100, 100, size=(M, K))
+        x = np.ldexp(rng.uniform(1.0, 2.0, size=(M, K)), e) * rng.choice([-1.0, 1.0], size=(M, K))
+        x[rng.random((M, K)) < 0.1] = 0.0
+        X = wl.to_bf16_bits(x)
+        check_stats(X, wl.gen_bf16(18, 2, 1, K)[0], 1e-6, f"wide {M}x{K}")
+
+
+def test_sum_of_squares_gaussian_rows_match_fsum():
+    """Ordinary activations (the fast path) and the 4096 x 7168 shape."""
+    X = wl.gen_bf16(19, 1, 64, 7168)
+    check_stats(X, wl.gen_bf16(19, 2, 1, 7168)[0], 1e-6, "gaussian 64x7168")
