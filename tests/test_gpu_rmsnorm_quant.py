@@ -180,3 +180,65 @@ def test_sum_of_squares_gaussian_rows_match_fsum():
     """Ordinary activations (the fast path) and the 4096 x 7168 shape."""
     X = wl.gen_bf16(19, 1, 64, 7168)
     check_stats(X, wl.gen_bf16(19, 2, 1, 7168)[0], 1e-6, "gaussian 64x7168")
+
+
+# ---------------------------------------------------------------- r decided
+def near_midpoint_rows(count, eps, seed=23, n=1 << 20):
+    """Rows of 32 values m * 2^-7 (|m| <= 255, exact in bf16; their sum of
+    squares is exact in fp64) whose r64 = 1 / sqrt(ss / 32 + eps) lies closest
+    to an fp32 rounding midpoint, found among n random rows; with n = 2^20 the
+    closest lie within ~2^-44 (relative) of a midpoint, well inside the band
+    where the kernel must fall back to the fp64 sequence."""
+    rng = np.random.default_rng(seed)
+    m = rng.integers(-255, 256, size=(n, 32), dtype=np.int32)
+    ss = (m * m).sum(axis=1).astype(np.float64) * 2.0 ** -14
+    e = float(np.float32(eps))
+    r64 = 1.0 / np.sqrt(ss / 32 + e)
+    c = r64.astype(np.float32)
+    up = np.nextafter(c, np.float32(np.inf)).astype(np.float64)
+    dn = np.nextafter(c, np.float32(0)).astype(np.float64)
+    c64 = c.astype(np.float64)
+    dist = np.minimum(np.abs(r64 - (c64 + up) / 2), np.abs(r64 - (c64 + dn) / 2)) / r64
+    pick = np.argsort(dist)[:count]
+    return m[pick].astype(np.float64) * 2.0 ** -7, dist[pick]
+
+
+@pytest.mark.parametrize("eps", [1e-6, 0.0, 3.0])
+def test_rstd_near_fp32_rounding_midpoints(eps):
+    """r equals RN32 of the fp64 sequence also when that value lies within
+    2^-38 of an fp32 rounding midpoint (the float-float estimate cannot decide
+    it there and the kernel takes the fp64 sequence)."""
+    x, dist = near_midpoint_rows(192, eps)
+    assert dist[0] < 2.0 ** -40 and (dist < 2.0 ** -37).sum() >= 16   # the band is exercised
+    X = wl.to_bf16_bits(x)
+    assert np.array_equal(oracle._bf16_bits_to_f64(X), x)
+    check_stats(X, wl.gen_bf16(24, 2, 1, 32)[0], eps, f"near midpoints eps={eps}")
+
+
+def test_rstd_extreme_scales():
+    """r across the fp32 range: rows near the bf16 maximum (r subnormal in
+    fp32, decided by the fp64 sequence), tiny rows with eps = 0 (r near
+    2^100), and eps dominating the row."""
+    K = 64
+    rows = [[1.5 * 2.0 ** 127] * 64, [1.0 * 2.0 ** 126] * 3, [2.0 ** 100, 3.0 * 2.0 ** 90],
+            [2.0 ** -90, -(2.0 ** -95)], [1.0, 2.0, 3.0], [2.0 ** -20] * 64]
+    X = np.stack([bf16_row(v, K) for v in rows])
+    for eps in (0.0, 1e-6, 1e30):
+        got = check_stats(X, wl.gen_bf16(25, 2, 1, K)[0], eps, f"extreme eps={eps}")
+        assert np.isfinite(got).all()
+
+
+def test_rstd_very_long_rows():
+    """K = 2^24: the estimate needs K < 2^24, so r comes from the fp64
+    sequence; the rows are taken in chunks of 8192 vectors."""
+    K = 1 << 24
+    x = wl.gen_bf16(26, 1, 2, K)
+    X = dev_bf16(x)
+    w = dev_bf16(wl.gen_bf16(26, 2, 1, K))[0].contiguous()
+    _, _, rstd, ss = mx.mxfp4_rmsnorm_quantize(X, w, 1e-6, stats=True)
+    torch.cuda.synchronize()
+    ss_ref = np.array([exact_sumsq(x[m]) for m in range(2)])
+    assert np.array_equal(host(ss).view(np.int64), ss_ref.view(np.int64))
+    e = float(np.float32(1e-6))
+    r_ref = np.array([np.float32(1.0 / math.sqrt(s / K + e)) for s in ss_ref], dtype=np.float32)
+    assert np.array_equal(host(rstd).view(np.int32), r_ref.view(np.int32))
