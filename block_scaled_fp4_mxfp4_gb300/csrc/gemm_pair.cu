@@ -22,9 +22,10 @@
 //                   rank 0 issues the MMAs
 //   warps 2, 3      lane 0 of rank 0 copies the stage's scale blocks into both
 //                   CTAs' TMEM (even / odd K blocks)
-//   warps 4-7       (both CTAs) epilogue: drain this CTA's accumulator rows,
-//                   hand TMEM back (arrive on rank 0's barrier), store C while
-//                   the next tile's mainloop runs
+//   warps 4-11      (both CTAs) epilogue: each drains 32 accumulator rows x
+//                   128 columns of this CTA into registers, hands TMEM back
+//                   (arrive on rank 0's barrier) and stores C while the next
+//                   tile's mainloop runs
 // MMA completion is signalled to both CTAs by multicast commits. Every wait
 // on an mbarrier is bounded; a final cluster barrier keeps both CTAs alive
 // until neither can touch the other's shared memory, then the pair frees its
