@@ -276,15 +276,13 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K)
     p.n_tiles = static_cast<int>((N + bn - 1) / bn);
     p.tiles = static_cast<int>(m_tiles * p.n_tiles);
     const int64_t k_stages = (K + 255) / 256;
+    // No K-split unless the measured table or an override asks for one: on
+    // GB300 one split was the fastest for every shape of the tuning sweep
+    // (M 128 / 256, N 512-7168, K 512-7168) and for long-K shapes with few
+    // tiles (16 x 640 x 4096, 128 x 2112 x 7168): summing fp32 partial tiles,
+    // through the workspace or through a cluster's shared memory (measured
+    // too), costs more than the shorter mainloop saves.
     int64_t s = 1;
-    if (2 * p.tiles <= kPlanSms && k_stages >= 4) {
-        s = kPlanSms / p.tiles;
-        if (s > k_stages / 2) s = k_stages / 2;
-        if (s > kMaxSplitK) s = kMaxSplitK;
-        // keep the fp32 partial traffic well below the weight bytes
-        while (s > 1 && s * M * N * 4 > N * (K / 2) / 2) --s;
-        if (s < 1) s = 1;
-    }
     const int want = split_choice(0, M, N, K);
     if (want > 0) {
         s = want;

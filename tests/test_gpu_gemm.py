@@ -118,3 +118,30 @@ def test_gemm_rejects_bad_arguments_without_launching():
     with pytest.raises(mx.Mxfp4Error) as e:
         mx.mxfp4_gemm_a4w4(qa, sf, qa, sf, 1000, C, mx.new_workspace(8, 8, 1024))
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("M,N,K,S", [(16, 640, 4096, 3), (200, 384, 2080, 6)])
+def test_gemm_workspace_split_k(M, N, K, S):
+    """K-splits (forced by the override; the planner picks one split unless its
+    table says otherwise) write fp32 partials to the workspace and the last
+    split to arrive sums them; with and without the epilogue extras."""
+    a, b = inputs(M, N, K, 400 + M + N + K)
+    qa, sfa, qa_r, sfa_r = quant_both(a)
+    qb, sfb, qb_r, sfb_r = quant_both(b)
+    c_in_bits = wl.gen_bf16(401 + M, 3, M, N)
+    old = mx.set_split_override("gemm", S)
+    try:
+        plan = mx.gemm_plan(M, N, K)
+        assert plan["kernel"] == "bs_gemm_kernel" and plan["splits"] == S, plan
+        C = mx.mxfp4_gemm_a4w4(qa, sfa, qb, sfb, K)
+        Ce = dev_bf16(c_in_bits).clone()
+        mx.mxfp4_gemm_a4w4_ex(qa, sfa, qb, sfb, K, Ce, alpha=0.5, beta=-1.0)
+        torch.cuda.synchronize()
+    finally:
+        mx.set_split_override("gemm", old)
+    c_ref, s = oracle.gemm_full(qa_r, sfa_r, qb_r, sfb_r, K, 32)
+    assert_within_tolerance(c_f64(C), c_ref, s, f"workspace split-K {S}: {M}x{N}x{K}")
+    c_in = wl.bf16_bits_to_float(c_in_bits).astype(np.float64)
+    ce_ref, se = oracle.gemm_epilogue(c_ref, s, 0.5, -1.0, c_in, None)
+    assert_within_tolerance(c_f64(Ce), ce_ref, se, f"workspace split-K {S} with epilogue")
+    assert mx.get_device_error() == 0

@@ -16,7 +16,7 @@ mx = pytest.importorskip("block_scaled_fp4_mxfp4_gb300.mxfp4")
 
 SHAPES = [
     ((130, 300, 96), "bs_gemm_kernel", 1),          # 128-wide tiles, ragged
-    ((16, 640, 4096), "bs_gemm_kernel", 2),         # split-K: epilogue in the final reduction
+    ((16, 640, 4096), "bs_gemm_kernel", 4),         # 4 K-splits (forced): epilogue in the final reduction
     ((1300, 1900, 320), "bs_gemm_kernel", 1),       # 256-wide tiles
     ((2100, 2100, 96), "bs_gemm_pair_kernel", 1),   # CTA pairs, ragged
 ]
@@ -32,12 +32,20 @@ def quant_pair(M, N, K, seed):
     return (qa, sfa, qb, sfb), (qa_r, sfa_r, qb_r, sfb_r)
 
 
-@pytest.mark.parametrize("shape,kernel,min_splits", SHAPES)
+@pytest.mark.parametrize("shape,kernel,splits", SHAPES)
 @pytest.mark.parametrize("alpha,beta,use_bias", [(0.5, -1.25, True), (2.0, 0.0, False), (1.0, 1.0, True)])
-def test_epilogue_matches_oracle(shape, kernel, min_splits, alpha, beta, use_bias):
+def test_epilogue_matches_oracle(shape, kernel, splits, alpha, beta, use_bias):
+    old = mx.set_split_override("gemm", splits if splits > 1 else 0)
+    try:
+        epilogue_case(shape, kernel, splits, alpha, beta, use_bias)
+    finally:
+        mx.set_split_override("gemm", old)
+
+
+def epilogue_case(shape, kernel, splits, alpha, beta, use_bias):
     M, N, K = shape
     plan = mx.gemm_plan(M, N, K)
-    assert plan["kernel"] == kernel and plan["splits"] >= min_splits
+    assert plan["kernel"] == kernel and plan["splits"] == splits, plan
     (qa, sfa, qb, sfb), (qa_r, sfa_r, qb_r, sfb_r) = quant_pair(M, N, K, 90 + M)
     c_in_bits = wl.gen_bf16(91 + M, 3, M, N)
     bias_bits = wl.gen_bf16(92 + M, 4, 1, N).reshape(N)

@@ -20,7 +20,8 @@ pytestmark = pytest.mark.gpu
 
 mx = pytest.importorskip("block_scaled_fp4_mxfp4_gb300.mxfp4")
 
-# (call, M, N, K, kernel the plan must name, range of the recorded code). The
+# (call, M, N, K, kernel the plan must name, range of the recorded code); the
+# split-K case forces 4 K-splits through the planner's override. The
 # fused shapes give each CTA more K-stages than its weight ring has slots, so
 # that its producer must wait for MMAs: a wait long enough for the GPU's
 # timer to see the limit pass (the fused kernel's other waits can all end
@@ -58,6 +59,14 @@ def make_call(kind, M, N, K):
 
 @pytest.mark.parametrize("name", list(CASES))
 def test_short_wait_limit_gives_up_cleanly_and_recovers(name):
+    old = mx.set_split_override("gemm", 4 if name == "gemm_splitk" else 0)
+    try:
+        wait_limit_case(name)
+    finally:
+        mx.set_split_override("gemm", old)
+
+
+def wait_limit_case(name):
     kind, M, N, K, kernel, (lo, hi) = CASES[name]
     plan = mx.gemm_plan(M, N, K, fused=kind != "gemm", nvfp4=kind == "fused_nv")
     assert plan["kernel"] == kernel, plan

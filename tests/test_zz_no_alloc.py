@@ -22,10 +22,19 @@ pytestmark = pytest.mark.gpu
 mx = pytest.importorskip("block_scaled_fp4_mxfp4_gb300.mxfp4")
 
 
-@pytest.mark.parametrize("M,N,K", [(16, 640, 4096),     # split-K: partials + tickets in the array
-                                   (130, 300, 96),       # ragged, no split
-                                   (64, 1000, 1536)])
-def test_noalloc_gemm_matches_regular_entry_point_twice(M, N, K):
+@pytest.mark.parametrize("M,N,K,splits", [(16, 640, 4096, 0),    # one split: tickets only
+                                          (16, 640, 4096, 3),    # split-K: partials + tickets in the array
+                                          (130, 300, 96, 0),     # ragged, no split
+                                          (64, 1000, 1536, 0)])
+def test_noalloc_gemm_matches_regular_entry_point_twice(M, N, K, splits):
+    old = mx.set_split_override("gemm", splits)
+    try:
+        run_noalloc_twice(M, N, K)
+    finally:
+        mx.set_split_override("gemm", old)
+
+
+def run_noalloc_twice(M, N, K):
     a = wl.gen_bf16(300 + M, 1, M, K)
     b = wl.gen_bf16(300 + M, 2, N, K)
     qa, sfa = mx.mxfp4_quantize(dev_bf16(a))
@@ -50,10 +59,18 @@ def test_noalloc_gemm_matches_regular_entry_point_twice(M, N, K):
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
-    """M=128, N=8192, K=16384 plans 4 K-splits: 16 MiB of partials > the 8 MiB array."""
+    """M=128, N=8192, K=16384 with 3 K-splits (forced by the override) plans
+    12.6 MB of partials > the 8 MiB array; the call is rejected on the host
+    (the plan is checked before the pointers are used)."""
     assert mx.lib().mxfp4_noalloc_scratch_bytes() == 8 << 20
     M, N, K = 128, 8192, 16384
-    aq = torch.zeros(16, dtype=torch.uint8, device="cuda")
-    status = mx.lib().mxfp4_gemm_a4w4_noalloc(aq.data_ptr(), K // 2, aq.data_ptr(), aq.data_ptr(), K // 2,
-                                              aq.data_ptr(), aq.data_ptr(), N, M, N, K, None)
+    old = mx.set_split_override("gemm", 3)
+    try:
+        plan = mx.gemm_plan(M, N, K)
+        assert plan["splits"] == 3, plan
+        aq = torch.zeros(16, dtype=torch.uint8, device="cuda")
+        status = mx.lib().mxfp4_gemm_a4w4_noalloc(aq.data_ptr(), K // 2, aq.data_ptr(), aq.data_ptr(), K // 2,
+                                                  aq.data_ptr(), aq.data_ptr(), N, M, N, K, None)
+    finally:
+        mx.set_split_override("gemm", old)
     assert status == 4  # MXFP4_ERR_WORKSPACE_TOO_SMALL, nothing enqueued
