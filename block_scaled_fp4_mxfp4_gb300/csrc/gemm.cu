@@ -463,8 +463,10 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
                 epilogue_bar();   // last_flag is reused by the next unit
             }
         }
-        // C stores by TMA have completed before the CTA leaves
-        if (Cfg::TMA_EPI && lane == 0) bulk_wait_all();
+        // the C stores by TMA have read their staging buffers before the CTA
+        // leaves (their writes complete with the grid, before any dependent
+        // grid's dependency wait returns)
+        if (Cfg::TMA_EPI && lane == 0) bulk_wait_read<0>();
     }
     __syncwarp();
 
