@@ -239,3 +239,26 @@ def test_rmsnorm_quantize_validation_needs_no_gpu():
     assert call_ex(18, None) == 3               # rstd 4-byte alignment
     assert call_ex(None, 20) == 3               # sumsq 8-byte alignment
     assert call_ex(None, None, w=None) == 1
+
+
+def test_split_table_is_well_formed_without_a_gpu():
+    """The measured K-split table the planner consults: unique (path, bucket,
+    N, K) keys, split counts the kernels accept (1-8 for the fused kernel's
+    clusters, 1-16 for the GEMM path), buckets the planner can produce, and
+    the sweep's grid fully covered for every path."""
+    t = mxfp4.split_table()
+    assert len(t) == 160
+    keys = {(e["path"], e["bucket"], e["n"], e["k"]) for e in t}
+    assert len(keys) == len(t)
+    for e in t:
+        assert e["path"] in ("gemm", "fused", "fused_nv"), e
+        if e["path"] == "gemm":
+            assert e["bucket"] in (1, 2) and 1 <= e["splits"] <= 16, e
+        else:
+            assert e["bucket"] in (16, 32, 64) and 1 <= e["splits"] <= 8, e
+        assert e["n"] in (512, 2112, 4096, 7168) and e["k"] in (512, 1024, 2048, 4096, 7168), e
+    for path, buckets in (("gemm", (1, 2)), ("fused", (16, 32, 64)), ("fused_nv", (16, 32, 64))):
+        got = {(e["bucket"], e["n"], e["k"]) for e in t if e["path"] == path}
+        assert got == {(b, n, k) for b in buckets for n in (512, 2112, 4096, 7168) for k in (512, 1024, 2048, 4096, 7168)}
+    # every GEMM-path entry keeps one split: the measured best everywhere
+    assert all(e["splits"] == 1 for e in t if e["path"] == "gemm")
