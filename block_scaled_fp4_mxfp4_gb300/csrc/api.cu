@@ -654,7 +654,7 @@ mxfp4_status_t mxfp4_quant_gemm_fused(const void *A, int64_t lda, const void *Bq
     uint8_t *w = static_cast<uint8_t *>(workspace);
     void *aq = w + wl.aq_off;
     void *asf = w + wl.sf_off;
-    st = cuda_status(launch_quant_mx(A, M, K, lda, aq, wl.ldq, asf, sms, s));
+    st = cuda_status(launch_quant_mx(A, M, K, lda, aq, wl.ldq, asf, sms, s, true));
     if (st != MXFP4_OK) return st;
     return run_gemm(aq, wl.ldq, asf, Bq, ldbq, B_sf, C, ldc, M, N, K, workspace, wl, s);
 }
@@ -753,7 +753,7 @@ mxfp4_status_t nvfp4_group_quant_gemm(const nvfp4_act_problem_t *problems, int n
     // one quantization launch per kMaxGroups groups
     for (int g0 = 0; g0 < num_groups; g0 += kMaxGroups) {
         st = cuda_status(launch_quant_nv_grouped(qg.data() + g0, std::min(kMaxGroups, num_groups - g0), sms,
-                                                 static_cast<cudaStream_t>(stream)));
+                                                 static_cast<cudaStream_t>(stream), g0 + kMaxGroups >= num_groups));
         if (st != MXFP4_OK) return st;
     }
     return group_gemm(q.data(), num_groups, true, w + wl.table_off, ws_bytes - wl.table_off, stream);

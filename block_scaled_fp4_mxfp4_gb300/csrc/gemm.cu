@@ -47,6 +47,29 @@ using namespace gemm_detail;
 
 __device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// 128-row chunks of the B tile n_tile that hold rows below N.
+template <class Cfg>
+__device__ __forceinline__ int valid_chunks(const GemmProblemDev &pr, int n_tile)
+{
+    int n = 0;
+#pragma unroll
+    for (int j = 0; j < Cfg::NCH; ++j)
+        if ((n_tile * Cfg::NCH + j) * 128 < pr.n) ++n;
+    return n;
+}
+
+// Bulk loads of one stage's B scale blocks (nblk blocks from blk0 of each
+// valid 128-row chunk) into the stage at st, completing on bar.
+template <class Cfg>
+__device__ __forceinline__ void load_b_scales(uint8_t *st, const GemmProblemDev &pr, int n_tile, int nch_valid, int blk0,
+                                              int nblk, uint64_t *bar, uint64_t pol)
+{
+    for (int j = 0; j < nch_valid; ++j)
+        bulk_load(st + Cfg::A_BYTES + Cfg::B_BYTES + Cfg::SFA_BYTES + j * Cfg::SF_BLK * 512,
+                  pr.sfb + (static_cast<size_t>(n_tile * Cfg::NCH + j) * pr.sf_cblocks + blk0) * 512, nblk * 512,
+                  bar, pol);
+}
+
 // One unit of work: an output tile, or one K-split of it.
 struct Unit {
     int g, tile, m_tile, n_tile, split, s_begin, nst;
@@ -106,6 +129,10 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int units = p.total_tiles * p.splits;
+    // stages of this CTA's first unit whose weights thread 0 requested before
+    // the grid-dependency wait (thread 0 is also the TMA producer)
+    int pre = 0;
+    const uint64_t pol_w = threadIdx.x == 0 ? policy_evict_last() : 0;
 
     if (threadIdx.x == 0) {
 #pragma unroll
@@ -127,12 +154,38 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
             tma_prefetch_desc(p.map_b(g));
             if (Cfg::TMA_EPI && p.problem(g).c_tma) tma_prefetch_desc(p.map_c(g));
         }
+        // Weights (B and its scales) are read-only inputs that no kernel of
+        // this library writes, so the first unit's first ring of weight
+        // stages is requested before the grid-dependency wait: under
+        // programmatic dependent launch it streams while the preceding grid
+        // (the quantization of A, in a quant -> GEMM call) finishes. Each
+        // stage's barriers are armed here for the whole stage; A and its
+        // scales follow once that grid has completed. Problems in a device
+        // table are read only after the wait.
+        if constexpr (!P::kTable) {
+            if (static_cast<int>(blockIdx.x) < units) {
+                const Unit w = decode_unit(p, blockIdx.x);
+                const GemmProblemDev &pr = p.problem(w.g);
+                const int nch_valid = valid_chunks<Cfg>(pr, w.n_tile);
+                pre = min(STAGES, w.nst);
+                for (int i = 0; i < pre; ++i) {
+                    const int ks = w.s_begin + i;
+                    const int blk0 = ks * Cfg::SF_BLK;
+                    const int nblk = min(Cfg::SF_BLK, pr.sf_cblocks - blk0);
+                    uint8_t *st = smem + i * Cfg::STAGE_BYTES;
+                    mbar_arrive_expect_tx(sf_data + i, (1 + nch_valid) * nblk * 512);
+                    load_b_scales<Cfg>(st, pr, w.n_tile, nch_valid, blk0, nblk, sf_data + i, pol_w);
+                    mbar_arrive_expect_tx(full + i, Cfg::A_BYTES + Cfg::B_BYTES);
+                    tma_load_2d(st + Cfg::A_BYTES, p.map_b(w.g), ks * 128, w.n_tile * BN, full + i, pol_w);
+                }
+            }
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
         tmem_relinquish();
     }
-    // every global access waits for the preceding grid in the stream
+    // every other global access waits for the preceding grid in the stream
     grid_dependency_wait();
     tc_fence_before();
     __syncthreads();
@@ -146,9 +199,12 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------------ TMA producer
-            const uint64_t pol = policy_evict_last();
+            const uint64_t pol = pol_w;
             int gs = 0, g_seen = -1;
-            for (int u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
+            // the first unit always runs: its stages below `pre` have weights
+            // in flight on armed barriers, which complete only once A follows
+            for (int u = blockIdx.x; u < units && (u == static_cast<int>(blockIdx.x) || !*abort_flag);
+                 u += gridDim.x) {
                 const Unit w = decode_unit(p, u);
                 const GemmProblemDev &pr = p.problem(w.g);
                 if (P::kTable && w.g != g_seen) {
@@ -156,10 +212,7 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
                     tma_desc_acquire(p.map_b(w.g));
                     g_seen = w.g;
                 }
-                int nch_valid = 0;
-#pragma unroll
-                for (int j = 0; j < Cfg::NCH; ++j)
-                    if ((w.n_tile * Cfg::NCH + j) * 128 < pr.n) ++nch_valid;
+                const int nch_valid = valid_chunks<Cfg>(pr, w.n_tile);
                 for (int i = 0; i < w.nst; ++i, ++gs) {
                     const int slot = gs % STAGES;
                     if (gs >= STAGES &&
@@ -171,19 +224,22 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
                     uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
                     const int blk0 = ks * Cfg::SF_BLK;
                     const int nblk = min(Cfg::SF_BLK, pr.sf_cblocks - blk0);
+                    // a stage below `pre` has its barriers armed and its weights
+                    // requested already (only in the first unit, where gs = i)
+                    const bool weights_sent = gs < pre;
                     // the scale blocks first, on their own barrier: their copy into
                     // TMEM then overlaps the arrival of the operand tiles
-                    mbar_arrive_expect_tx(sf_data + slot, (1 + nch_valid) * nblk * 512);
+                    if (!weights_sent) mbar_arrive_expect_tx(sf_data + slot, (1 + nch_valid) * nblk * 512);
                     bulk_load(st + Cfg::A_BYTES + Cfg::B_BYTES,
                               pr.sfa + (static_cast<size_t>(w.m_tile) * pr.sf_cblocks + blk0) * 512, nblk * 512,
                               sf_data + slot, pol);
-                    for (int j = 0; j < nch_valid; ++j)
-                        bulk_load(st + Cfg::A_BYTES + Cfg::B_BYTES + Cfg::SFA_BYTES + j * Cfg::SF_BLK * 512,
-                                  pr.sfb + (static_cast<size_t>(w.n_tile * Cfg::NCH + j) * pr.sf_cblocks + blk0) * 512,
-                                  nblk * 512, sf_data + slot, pol);
-                    mbar_arrive_expect_tx(full + slot, Cfg::A_BYTES + Cfg::B_BYTES);
+                    if (!weights_sent) {
+                        load_b_scales<Cfg>(st, pr, w.n_tile, nch_valid, blk0, nblk, sf_data + slot, pol);
+                        mbar_arrive_expect_tx(full + slot, Cfg::A_BYTES + Cfg::B_BYTES);
+                    }
                     tma_load_2d(st, p.map_a(w.g), ks * 128, w.m_tile * 128, full + slot, pol);
-                    tma_load_2d(st + Cfg::A_BYTES, p.map_b(w.g), ks * 128, w.n_tile * BN, full + slot, pol);
+                    if (!weights_sent)
+                        tma_load_2d(st + Cfg::A_BYTES, p.map_b(w.g), ks * 128, w.n_tile * BN, full + slot, pol);
                     issued = gs + 1;
                 }
             }
@@ -366,12 +422,40 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
                 tc_fence_before();
                 mbar_arrive(acc_empty);
                 if (Cfg::TMA_EPI && pr.c_tma) {
-                    // 32 x 32 sub-tiles (this warp's 32 rows) through the warp's two
-                    // staging buffers, written by TMA: each lane writes its row's 64
-                    // bytes in the 64-byte-swizzled layout of the tensor map (16-byte
-                    // chunk j of row r at chunk j ^ ((r / 2) % 4)); the map clips rows
-                    // past M and columns past N
-                    if (run) {
+                    // 32 x 32 sub-tiles of this warp's 32 rows, written by TMA from
+                    // shared memory: each lane writes its row's 64 bytes in the
+                    // 64-byte-swizzled layout of the tensor map (16-byte chunk j of
+                    // row r at chunk j ^ ((r / 2) % 4)); the map clips rows past M
+                    // and columns past N.
+                    auto stage_subtile = [&](uint8_t *buf, int c) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            *reinterpret_cast<uint4 *>(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                                make_uint4(pk[c * 16 + 4 * j], pk[c * 16 + 4 * j + 1], pk[c * 16 + 4 * j + 2],
+                                           pk[c * 16 + 4 * j + 3]);
+                    };
+                    if (P::kTable && run && lane == 0) tma_desc_acquire(p.map_c(w.g));
+                    if (run && u + static_cast<int>(gridDim.x) >= units) {
+                        // The CTA's last unit: the stage ring is free (every MMA
+                        // that read it has completed), so all sub-tiles are staged
+                        // there at once, behind one proxy fence (a fence and a
+                        // store issue cost ~0.1 us per sub-tile, measured).
+#pragma unroll
+                        for (int c = 0; c < BN / 32; ++c) stage_subtile(smem + (q * (BN / 32) + c) * 2048, c);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            for (int c = 0; c < BN / 32; ++c) {
+                                const int col0 = w.n_tile * BN + c * 32;
+                                if (col0 < pr.n)
+                                    tma_store_2d(p.map_c(w.g), smem + (q * (BN / 32) + c) * 2048, col0,
+                                                 w.m_tile * 128 + q * 32);
+                            }
+                            bulk_commit();
+                        }
+                    } else if (run) {
+                        // otherwise through the warp's two staging buffers, while
+                        // the next unit's mainloop uses the ring
 #pragma unroll
                         for (int c = 0; c < BN / 32; ++c) {
                             const int col0 = w.n_tile * BN + c * 32;
@@ -381,15 +465,10 @@ __global__ void __launch_bounds__(256, 1) bs_gemm_kernel(const __grid_constant__
                                     if (lane == 0) bulk_wait_read<1>();   // the buffer's previous store has read it
                                     __syncwarp();
                                 }
-#pragma unroll
-                                for (int j = 0; j < 4; ++j)
-                                    *reinterpret_cast<uint4 *>(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
-                                        make_uint4(pk[c * 16 + 4 * j], pk[c * 16 + 4 * j + 1], pk[c * 16 + 4 * j + 2],
-                                                   pk[c * 16 + 4 * j + 3]);
+                                stage_subtile(buf, c);
                                 fence_proxy_async_smem();
                                 __syncwarp();
                                 if (lane == 0) {
-                                    if (P::kTable && c == 0) tma_desc_acquire(p.map_c(w.g));
                                     tma_store_2d(p.map_c(w.g), buf, col0, w.m_tile * 128 + q * 32);
                                     bulk_commit();
                                 }

@@ -64,8 +64,14 @@ cudaError_t prepare_kernel(Kern kern, uint32_t smem_bytes, KernelOnce &once, int
 }
 
 // ---------------------------------------------------------------- quant.cu
+// Every quantization launch uses programmatic dependent launch and reads A
+// only after the preceding grid has completed. feeds_gemm: the next launch
+// is this library's GEMM on the quantized activations, which may start once
+// every CTA has passed that wait (it reads only weights before its own
+// wait); otherwise the next grid starts when this one has exited, and the
+// codes and scales are made visible device-wide before each CTA exits.
 cudaError_t launch_quant_mx(const void *A, int64_t M, int64_t K, int64_t lda, void *Aq,
-                            int64_t ldq, void *sf, int num_sms, cudaStream_t stream);
+                            int64_t ldq, void *sf, int num_sms, cudaStream_t stream, bool feeds_gemm = false);
 cudaError_t launch_quant_nv(const void *A, int64_t M, int64_t K, int64_t lda, void *Aq,
                             int64_t ldq, void *sf, int num_sms, cudaStream_t stream);
 // One matrix of a grouped NVFP4 quantization (bf16 A [M, K] -> packed codes
@@ -78,7 +84,8 @@ struct QuantGroupHost {
     void *sf;
 };
 // All `count` (1..kMaxGroups) matrices in one launch.
-cudaError_t launch_quant_nv_grouped(const QuantGroupHost *groups, int count, int num_sms, cudaStream_t stream);
+cudaError_t launch_quant_nv_grouped(const QuantGroupHost *groups, int count, int num_sms, cudaStream_t stream,
+                                    bool feeds_gemm = false);
 
 // --------------------------------------------------------- rmsnorm_quant.cu
 // Fused RMSNorm (bf16 weight [K], eps) + MXFP4 quantization of bf16 X [M, K].

@@ -50,6 +50,7 @@ struct QuantGroupsDev {
     int M[kMaxGroups], K[kMaxGroups], nchunk[kMaxGroups];
     int vec_store[kMaxGroups];   // code rows 16-byte aligned: one vector store per lane
     int count;
+    int feeds_gemm;              // let the next grid start right after the dependency wait
 };
 
 // Position of 16-byte slot s of a warp's chunk buffer: the slot's bank group
@@ -64,6 +65,12 @@ __global__ void __launch_bounds__(kQuantThreads, kQuantBlocksPerSm<VEC>) quant_k
     constexpr int BPL = 32 / VEC;                 // blocks per lane (1 or 2)
     constexpr uint32_t PAD = VEC == 32 ? 0x7Fu : 0x00u;
     __shared__ uint4 chunk_buf[kQuantWarps][kChunk / 8];
+    // Launched with programmatic dependent launch: A is read only after the
+    // preceding grid has completed. The GEMM of a quant -> GEMM call may
+    // start right after that and request its weights; it reads what this
+    // grid writes only after its own dependency wait.
+    grid_dependency_wait();
+    if (q.feeds_gemm) grid_launch_dependents();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     uint4 *buf = chunk_buf[warp];
@@ -141,15 +148,20 @@ __global__ void __launch_bounds__(kQuantThreads, kQuantBlocksPerSm<VEC>) quant_k
                                           ((r >> 5) & 3) * 4) = word;
         }
     }
+    // A grid that starts when this one has exited (the implicit trigger) may
+    // read weights quantized here before its dependency wait: the codes and
+    // scales are performed device-wide before the CTA leaves.
+    __threadfence();
 }
 
 template <int VEC>
-cudaError_t launch_quant(const QuantGroupHost *groups, int count, int num_sms, cudaStream_t stream)
+cudaError_t launch_quant(const QuantGroupHost *groups, int count, int num_sms, cudaStream_t stream, bool feeds_gemm)
 {
     if (count < 1 || count > kMaxGroups) return cudaErrorInvalidValue;
     QuantGroupsDev q;
     memset(&q, 0, sizeof(q));
     q.count = count;
+    q.feeds_gemm = feeds_gemm ? 1 : 0;
     q.first[0] = 0;
     for (int g = 0; g < count; ++g) {
         const QuantGroupHost &h = groups[g];
@@ -171,29 +183,39 @@ cudaError_t launch_quant(const QuantGroupHost *groups, int count, int num_sms, c
     const int64_t cap = static_cast<int64_t>(num_sms) * kQuantBlocksPerSm<VEC>;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    quant_kernel<VEC><<<static_cast<unsigned>(blocks), kQuantThreads, 0, stream>>>(q);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+    cfg.blockDim = dim3(kQuantThreads, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, quant_kernel<VEC>, q);
 }
 
 }  // namespace
 
-cudaError_t launch_quant_nv_grouped(const QuantGroupHost *groups, int count, int num_sms, cudaStream_t stream)
+cudaError_t launch_quant_nv_grouped(const QuantGroupHost *groups, int count, int num_sms, cudaStream_t stream,
+                                    bool feeds_gemm)
 {
-    return launch_quant<16>(groups, count, num_sms, stream);
+    return launch_quant<16>(groups, count, num_sms, stream, feeds_gemm);
 }
 
 cudaError_t launch_quant_mx(const void *A, int64_t M, int64_t K, int64_t lda, void *Aq,
-                            int64_t ldq, void *sf, int num_sms, cudaStream_t stream)
+                            int64_t ldq, void *sf, int num_sms, cudaStream_t stream, bool feeds_gemm)
 {
     const QuantGroupHost one{A, M, K, lda, Aq, ldq, sf};
-    return launch_quant<32>(&one, 1, num_sms, stream);
+    return launch_quant<32>(&one, 1, num_sms, stream, feeds_gemm);
 }
 
 cudaError_t launch_quant_nv(const void *A, int64_t M, int64_t K, int64_t lda, void *Aq,
                             int64_t ldq, void *sf, int num_sms, cudaStream_t stream)
 {
     const QuantGroupHost one{A, M, K, lda, Aq, ldq, sf};
-    return launch_quant<16>(&one, 1, num_sms, stream);
+    return launch_quant<16>(&one, 1, num_sms, stream, false);
 }
 
 }  // namespace mxfp4

@@ -43,13 +43,19 @@
  *   MXFP4_ERR_CUDA. There is no fallback path of any kind.
  * - Thread safety: calls may come from several host threads; the internal
  *   plan cache is locked.
- * - Overlap of consecutive calls: GEMM launches use programmatic dependent
- *   launch. A call may start while the preceding kernel in the stream is
- *   finishing and may already read its pre-quantized weights (Bq, B_sf) then;
- *   A, C, the workspace and every write wait until the preceding kernel has
- *   completed. Only this library's GEMM kernels let a successor start early,
- *   and they never write weight buffers, so stream order is preserved as
- *   long as weights are not produced by a GEMM call of this library.
+ * - Overlap of consecutive calls: GEMM and quantization launches use
+ *   programmatic dependent launch. A GEMM call may start before the
+ *   preceding kernel in the stream has completed and may already read its
+ *   pre-quantized weights (Bq, B_sf) then; A, C, the workspace and every
+ *   write wait until the preceding kernel has completed. A kernel of this
+ *   library lets its successor start early only after its own wait for its
+ *   predecessor, and a quantization kernel makes its codes and scales visible
+ *   device-wide before it exits, so weights written by this library's
+ *   quantization calls, or by work enqueued before the preceding kernel, are
+ *   read in stream order. Weights written by some other kernel launched
+ *   directly before a GEMM call on the same stream need an event or a copy
+ *   between the two: that kernel's writes are guaranteed visible to a
+ *   dependent launch only once the dependent grid has waited for it.
  */
 #ifndef MXFP4_GB300_H
 #define MXFP4_GB300_H
