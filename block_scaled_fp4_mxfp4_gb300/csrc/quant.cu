@@ -150,8 +150,9 @@ __global__ void __launch_bounds__(kQuantThreads, kQuantBlocksPerSm<VEC>) quant_k
     }
     // A grid that starts when this one has exited (the implicit trigger) may
     // read weights quantized here before its dependency wait: the codes and
-    // scales are performed device-wide before the CTA leaves.
-    __threadfence();
+    // scales are performed device-wide before the CTA leaves. (The GEMM that
+    // a quant -> GEMM call releases early reads them only after its wait.)
+    if (!q.feeds_gemm) __threadfence();
 }
 
 template <int VEC>
