@@ -128,6 +128,23 @@ __device__ __forceinline__ PairUnit decode_pair_unit(const P &p, int u)
     return w;
 }
 
+// Weight half of stage i (K stage i) of pair tile w for CTA `rank`: the scale
+// blocks of both 128-row chunks of the tile's B (completing rank 0's scale
+// barrier at sf_bar) and this CTA's 128 rows of B (rank 0's operand barrier
+// at full_bar).
+template <class Cfg, class P>
+__device__ __forceinline__ void load_b_stage(const P &p, const PairUnit &w, const GemmProblemDev &pr, uint32_t rank,
+                                             int i, uint8_t *st, uint32_t full_bar, uint32_t sf_bar, uint64_t pol)
+{
+    const int blk0 = i * Cfg::SF_BLK;
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+        tma_load_2d_pair(st + Cfg::A_BYTES + Cfg::B_BYTES + Cfg::SFA_BYTES + j * Cfg::SF_BLK * 512, p.map_sfb(w.g), 0,
+                         (w.n_tile * 2 + j) * pr.sf_cblocks + blk0, sf_bar, pol);
+    tma_load_2d_pair(st + Cfg::A_BYTES, p.map_b(w.g), i * 128, w.n_tile * 256 + static_cast<int>(rank) * 128, full_bar,
+                     pol);
+}
+
 // EPI: the variant with the alpha / beta / bias epilogue (mxfp4_gemm_a4w4_ex).
 // P: PairParams<MAXG> (problems in kernel parameters) or PairParamsTable.
 template <int KIND, int STAGES, class P, bool F16, bool EPI = false>
@@ -183,11 +200,37 @@ __global__ void __launch_bounds__(kPairThreads, 1) bs_gemm_pair_kernel(const __g
         tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
         tmem_relinquish_pair();
     }
-    // every global access waits for the preceding grid in the stream
-    grid_dependency_wait();
+    // both CTAs' barriers exist before any arrival from the other CTA
     tc_fence_before();
-    cluster_sync();   // both CTAs' barriers exist before any arrival from the other CTA
+    cluster_sync();
     tc_fence_after();
+    // Weights (B and its scales) are read-only inputs that no kernel of this
+    // library writes, so each CTA requests its half of the first pair tile's
+    // first ring of weight stages before the grid-dependency wait (rank 0
+    // arms those stages for all of their bytes); A and its scales follow once
+    // the preceding grid has completed. Problems in a device table are read
+    // only after the wait.
+    int pre = 0;   // stages of the first pair tile whose weights are requested (thread 0)
+    const uint64_t pol = policy_evict_last();
+    if constexpr (!P::kTable) {
+        if (threadIdx.x == 0 && pair < units) {
+            const PairUnit w = decode_pair_unit(p, pair);
+            const GemmProblemDev &pr = p.problem(w.g);
+            pre = min(STAGES, (pr.k + 255) / 256);
+            const uint32_t full_r0 = mapa_shared(smem_u32(full), 0);
+            const uint32_t sf_r0 = mapa_shared(smem_u32(sf_data), 0);
+            for (int i = 0; i < pre; ++i) {
+                uint8_t *st = smem + i * Cfg::STAGE_BYTES;
+                if (leader) {
+                    mbar_arrive_expect_tx(sf_data + i, 2 * (Cfg::SFA_BYTES + Cfg::SFB_BYTES));
+                    mbar_arrive_expect_tx(full + i, 2 * (Cfg::A_BYTES + Cfg::B_BYTES));
+                }
+                load_b_stage<Cfg>(p, w, pr, rank, i, st, full_r0 + i * 8, sf_r0 + i * 8, pol);
+            }
+        }
+    }
+    // every other global access waits for the preceding grid in the stream
+    grid_dependency_wait();
     grid_launch_dependents();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tmem_acc = tmem;
@@ -204,11 +247,13 @@ __global__ void __launch_bounds__(kPairThreads, 1) bs_gemm_pair_kernel(const __g
             // after the MMAs that needed rank 0's previous phase of it.
             // Boxes past the last row or scale block read zeros and still count
             // their full size.
-            const uint64_t pol = policy_evict_last();
             const uint32_t full_r0 = mapa_shared(smem_u32(full), 0);
             const uint32_t sf_r0 = mapa_shared(smem_u32(sf_data), 0);
             int gs = 0, g_seen = -1;
-            for (int u = pair; u < units && !*abort_flag; u += npairs) {
+            // the first pair tile always runs: its stages below `pre` have
+            // weights in flight on armed barriers, which complete only once A
+            // follows
+            for (int u = pair; u < units && (u == pair || !*abort_flag); u += npairs) {
                 const PairUnit w = decode_pair_unit(p, u);
                 const GemmProblemDev &pr = p.problem(w.g);
                 if (P::kTable && w.g != g_seen) {
@@ -229,21 +274,18 @@ __global__ void __launch_bounds__(kPairThreads, 1) bs_gemm_pair_kernel(const __g
                     }
                     uint8_t *st = smem + slot * Cfg::STAGE_BYTES;
                     const int blk0 = i * Cfg::SF_BLK;
-                    if (leader) {
+                    // a stage below `pre` has its barriers armed and its weights
+                    // requested already (only in the first pair tile, where gs = i)
+                    const bool weights_sent = gs < pre;
+                    if (leader && !weights_sent) {
                         mbar_arrive_expect_tx(sf_data + slot, 2 * (Cfg::SFA_BYTES + Cfg::SFB_BYTES));
                         mbar_arrive_expect_tx(full + slot, 2 * (Cfg::A_BYTES + Cfg::B_BYTES));
                     }
                     // the scale blocks first, on their own barrier
                     tma_load_2d_pair(st + Cfg::A_BYTES + Cfg::B_BYTES, p.map_sfa(w.g), 0, a_chunk * pr.sf_cblocks + blk0,
                                      sf_r0 + slot * 8, pol);
-#pragma unroll
-                    for (int j = 0; j < 2; ++j)
-                        tma_load_2d_pair(st + Cfg::A_BYTES + Cfg::B_BYTES + Cfg::SFA_BYTES + j * Cfg::SF_BLK * 512,
-                                         p.map_sfb(w.g), 0, (w.n_tile * 2 + j) * pr.sf_cblocks + blk0, sf_r0 + slot * 8,
-                                         pol);
+                    if (!weights_sent) load_b_stage<Cfg>(p, w, pr, rank, i, st, full_r0 + slot * 8, sf_r0 + slot * 8, pol);
                     tma_load_2d_pair(st, p.map_a(w.g), i * 128, a_chunk * 128, full_r0 + slot * 8, pol);
-                    tma_load_2d_pair(st + Cfg::A_BYTES, p.map_b(w.g), i * 128,
-                                     w.n_tile * 256 + static_cast<int>(rank) * 128, full_r0 + slot * 8, pol);
                     issued = gs + 1;
                 }
             }
