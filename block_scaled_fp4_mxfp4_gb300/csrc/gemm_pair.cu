@@ -84,6 +84,7 @@ struct PairParams {
     int total_tiles;
     uint64_t wait_ns;          // limit of the waits that guard work
     static constexpr bool kTable = false;
+    static constexpr bool kColumnsFastest = MAXG == 1;   // tile order of a single problem
     __device__ __forceinline__ const CUtensorMap *map_a(int g) const { return &tma[g]; }
     __device__ __forceinline__ const CUtensorMap *map_b(int g) const { return &tmb[g]; }
     __device__ __forceinline__ const CUtensorMap *map_sfa(int g) const { return &tmsfa[g]; }
@@ -100,6 +101,7 @@ struct PairParamsTable {
     int total_tiles;
     uint64_t wait_ns;
     static constexpr bool kTable = true;
+    static constexpr bool kColumnsFastest = false;
     __device__ __forceinline__ const CUtensorMap *map_a(int g) const { return maps + g * kTableMaps; }
     __device__ __forceinline__ const CUtensorMap *map_b(int g) const { return maps + g * kTableMaps + 1; }
     __device__ __forceinline__ const CUtensorMap *map_sfa(int g) const { return maps + g * kTableMaps + 2; }
@@ -114,7 +116,9 @@ struct PairUnit {
     int g, m_pair, n_tile;
 };
 
-// Pair tiles are numbered group by group, 256-row tiles fastest.
+// Pair tiles are numbered group by group, 256-row tiles fastest, except in a
+// launch of one problem, where 256-column tiles go fastest (measured at
+// 8192^3: 177.3 against 178.4 us; grouped lists ran 0.1-0.4 us slower with it).
 template <class P>
 __device__ __forceinline__ PairUnit decode_pair_unit(const P &p, int u)
 {
@@ -123,8 +127,13 @@ __device__ __forceinline__ PairUnit decode_pair_unit(const P &p, int u)
     w.g = g;
     const GemmProblemDev &pr = p.problem(g);
     const int local = u - pr.tile_start;
-    w.m_pair = local % pr.m_tiles;
-    w.n_tile = local / pr.m_tiles;
+    if constexpr (P::kColumnsFastest) {
+        w.n_tile = local % pr.n_tiles;
+        w.m_pair = local / pr.n_tiles;
+    } else {
+        w.m_pair = local % pr.m_tiles;
+        w.n_tile = local / pr.m_tiles;
+    }
     return w;
 }
 
