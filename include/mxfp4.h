@@ -40,7 +40,11 @@
  *   only element alignment.
  * - Errors: arguments are checked on the host before anything is enqueued; a
  *   non-OK status means nothing was launched. A failed launch returns
- *   MXFP4_ERR_CUDA. There is no fallback path of any kind.
+ *   MXFP4_ERR_CUDA. There is no fallback path of any kind. Every call below
+ *   that launches a kernel can also fail on the device after returning
+ *   MXFP4_OK: a kernel that gives up a bounded wait leaves that call's
+ *   outputs unspecified and reports it only through mxfp4_get_device_error,
+ *   which a caller whose results matter checks after synchronizing.
  * - Thread safety: calls may come from several host threads; the internal
  *   plan cache is locked.
  * - Overlap of consecutive calls: GEMM and quantization launches use
