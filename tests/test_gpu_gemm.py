@@ -40,6 +40,10 @@ GEMM_SHAPES = [
     # pairs take a second tile); then ragged M (the second CTA of the last tile row
     # has no rows), ragged N (no second B half) and K = 96 (half an MMA step of zeros)
     (2560, 2048, 128), (2100, 2100, 96),
+    # 81 pair tiles = 76 + 5: a second wave of five tiles on the ragged last tile
+    # row (its last tile 152 columns wide, the second CTA with 124 rows), K of
+    # five stages, the last one partial
+    (2300, 2200, 1056),
 ]
 
 
@@ -59,6 +63,7 @@ FUSED_SHAPES = [
     (1, 128, 256), (8, 512, 1024), (16, 2112, 7168), (16, 200, 96), (5, 130, 4128),
     (17, 384, 768), (32, 256, 2048), (33, 300, 512), (64, 640, 1024),      # fused small-M path
     (65, 256, 512), (130, 300, 96), (256, 512, 2048),                       # quant -> GEMM path
+    (2300, 2200, 1056),                                                     # ... on CTA pairs, ragged edges
 ]
 
 
