@@ -34,6 +34,9 @@ namespace {
 constexpr int kQuantThreads = 256;
 constexpr int kQuantWarps = kQuantThreads / 32;
 constexpr int kChunk = 1024;            // elements per work unit (one warp)
+// A of at most this many bytes is prefetched into L2 before the dependency
+// wait (a larger one would only double the requests of the loads that follow)
+constexpr int64_t kQuantPrefetchMaxBytes = 16ll << 20;
 // resident blocks per SM (16 KB of shared memory each): MXFP4 fits in 40
 // registers, NVFP4's reciprocal and scale conversion want a few more
 template <int VEC>
@@ -51,6 +54,7 @@ struct QuantGroupsDev {
     int vec_store[kMaxGroups];   // code rows 16-byte aligned: one vector store per lane
     int count;
     int feeds_gemm;              // let the next grid start right after the dependency wait
+    int prefetch;                // A is small: pull it into L2 before the dependency wait
 };
 
 // Position of 16-byte slot s of a warp's chunk buffer: the slot's bank group
@@ -65,17 +69,33 @@ __global__ void __launch_bounds__(kQuantThreads, kQuantBlocksPerSm<VEC>) quant_k
     constexpr int BPL = 32 / VEC;                 // blocks per lane (1 or 2)
     constexpr uint32_t PAD = VEC == 32 ? 0x7Fu : 0x00u;
     __shared__ uint4 chunk_buf[kQuantWarps][kChunk / 8];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t units = q.first[q.count];
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kQuantWarps;
+    if (q.prefetch && lane == 0) {
+        // A small A is requested into L2 while the preceding grid still runs
+        // (this grid starts early under programmatic dependent launch): the
+        // loads after the wait then hit L2. L2 is the point of coherence, so
+        // a later write of the preceding grid still reaches those loads.
+        int g = 0;
+        for (int64_t u = static_cast<int64_t>(blockIdx.x) * kQuantWarps + warp; u < units; u += nwarps) {
+            while (u >= q.first[g + 1]) ++g;
+            const int64_t local = u - q.first[g];
+            const int nch = q.nchunk[g];
+            const int64_t r = local / nch;
+            const int k0 = static_cast<int>(local - r * nch) * kChunk;
+            if (r < q.M[g])
+                prefetch_l2_bulk(q.A[g] + r * q.lda[g] + k0, static_cast<uint32_t>(min(kChunk, q.K[g] - k0) * 2));
+        }
+    }
     // Launched with programmatic dependent launch: A is read only after the
     // preceding grid has completed. The GEMM of a quant -> GEMM call may
     // start right after that and request its weights; it reads what this
     // grid writes only after its own dependency wait.
     grid_dependency_wait();
     if (q.feeds_gemm) grid_launch_dependents();
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
     uint4 *buf = chunk_buf[warp];
-    const int64_t units = q.first[q.count];
-    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kQuantWarps;
     int g = 0;
     for (int64_t u = static_cast<int64_t>(blockIdx.x) * kQuantWarps + warp; u < units; u += nwarps) {
         while (u >= q.first[g + 1]) ++g;         // units only grow along the loop
@@ -163,6 +183,7 @@ cudaError_t launch_quant(const QuantGroupHost *groups, int count, int num_sms, c
     memset(&q, 0, sizeof(q));
     q.count = count;
     q.feeds_gemm = feeds_gemm ? 1 : 0;
+    int64_t a_bytes = 0;
     q.first[0] = 0;
     for (int g = 0; g < count; ++g) {
         const QuantGroupHost &h = groups[g];
@@ -177,7 +198,9 @@ cudaError_t launch_quant(const QuantGroupHost *groups, int count, int num_sms, c
         q.nchunk[g] = static_cast<int>((h.K + kChunk - 1) / kChunk);
         q.vec_store[g] = ((reinterpret_cast<uintptr_t>(h.Aq) & 15u) == 0 && (h.ldq & 15) == 0) ? 1 : 0;
         q.first[g + 1] = q.first[g] + (h.M + 127) / 128 * 128 * q.nchunk[g];
+        a_bytes += h.M * h.K * 2;
     }
+    q.prefetch = a_bytes <= kQuantPrefetchMaxBytes ? 1 : 0;
     for (int g = count + 1; g <= kMaxGroups; ++g) q.first[g] = q.first[count];
     const int64_t units = q.first[count];
     int64_t blocks = (units + kQuantWarps - 1) / kQuantWarps;
