@@ -17,7 +17,9 @@
 //                  per row = 128 bytes per stage) and, first and on their own
 //                  barrier, the stage's 512-byte scale blocks (1-D bulk copies
 //                  straight from the blocked layout: consecutive K-blocks of
-//                  128 rows are contiguous).
+//                  128 rows are contiguous). The weights of the first tile's
+//                  first ring of stages are requested before the grid-
+//                  dependency wait.
 //   warp 1         allocates TMEM; lane 0 issues the four K = 64 MMAs of each
 //                  stage and commits the stage's "empty" barrier.
 //   warps 2, 3     lane 0 of each copies half of every stage's scale blocks

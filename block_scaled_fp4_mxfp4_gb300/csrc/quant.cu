@@ -21,7 +21,10 @@
 // past M up to the next multiple of 128 and K-blocks past K inside a written
 // word get the pad byte (0x7F for E8M0 = 1.0, 0x00 for E4M3). One launch may
 // quantize up to kMaxGroups matrices (the grouped path); a single matrix is a
-// table of one.
+// table of one. Launches use programmatic dependent launch: A is read after
+// the wait for the preceding grid (a small A is prefetched into L2 before
+// it), and inside a quant -> GEMM call the GEMM is released right after that
+// wait so that it streams its weights while A is quantized.
 #include <cstring>
 
 #include "internal.h"
